@@ -1,0 +1,498 @@
+"""Benchmark of the Q4_0 quantized linear layer on GB300.
+
+Headline workload: the decode GEMV of a 4B-class FFN up-projection,
+m = 1 token, n = 9728 output rows, k = 2560 inputs, W in Q4_0 (14,008,320
+bytes of blocks). One step is one q4_0_matmul call on fresh weights: the
+step cycles through enough distinct packed copies of W that their total is
+more than twice the 129 MB L2, so every step reads its weights from HBM.
+Steps run as CUDA-graph replays; the timed region is bracketed by CUDA
+events on the launching stream with a synchronize on both sides.
+
+Printed: one JSON line (rank 0). `value` is weight GB/s over all ranks;
+`roofline` compares the decode kernel with the measured HBM copy bandwidth;
+`e2e` is the same metric through the public API with pinned host buffers
+and the per-step host<->device copies inside the timed region;
+`cpu_baseline` times the CPU oracle on the host cores on a bounded sample;
+`sweep` reports the other workload shapes (parity-tested elsewhere).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                  [--no-sweep] [--no-cpu]
+
+With --gpus N > 1 (torchrun) every rank runs an independent replica of the
+workload on its own GPU (the layer has no exchange step); the time is the
+maximum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4_0 weight GB/s (% HBM peak) at m=1..16; prefill TFLOP/s (% bf16 peak)"
+L2_BYTES = 129 * 1024 * 1024
+HEADLINE = dict(name="decode GEMV, FFN up-projection", m=1, n=9728, k=2560)
+WORKLOADS = {
+    "decode": HEADLINE,
+    "gemv1k": dict(name="single GEMV", m=1, n=1024, k=1024),
+    "slots4-up": dict(name="4 slots, up-projection", m=4, n=9728, k=2560),
+    "slots4-down": dict(name="4 slots, down-projection", m=4, n=2560, k=9728),
+    **{f"sweep-m{m}": dict(name="slot sweep 14336x4096", m=m, n=14336, k=4096) for m in (1, 2, 4, 8, 16)},
+    "logit": dict(name="logit head", m=4, n=151936, k=2560),
+    "prefill": dict(name="prefill", m=540, n=9728, k=2560),
+}
+SWEEP = [
+    dict(name="single GEMV", m=1, n=1024, k=1024),
+    dict(name="decode up-projection", m=1, n=9728, k=2560),
+    dict(name="4 slots, up-projection", m=4, n=9728, k=2560),
+    dict(name="4 slots, down-projection", m=4, n=2560, k=9728),
+    dict(name="slot sweep 14336x4096", m=1, n=14336, k=4096),
+    dict(name="slot sweep 14336x4096", m=2, n=14336, k=4096),
+    dict(name="slot sweep 14336x4096", m=4, n=14336, k=4096),
+    dict(name="slot sweep 14336x4096", m=8, n=14336, k=4096),
+    dict(name="slot sweep 14336x4096", m=16, n=14336, k=4096),
+    dict(name="logit head", m=4, n=151936, k=2560),
+    dict(name="prefill", m=540, n=9728, k=2560),
+]
+
+
+def weight_bytes(n, k):
+    return n * (k // 32) * 18
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "q4_quantized_linear_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kind}.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    mh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_source_hash():
+        return None
+    return float(mt.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU --
+
+class Workload:
+    """Packed weight copies, X and Y resident on the GPU for one shape."""
+
+    def __init__(self, q4lib, m, n, k, min_copies=1):
+        import torch
+        from q4_quantized_linear_gb300 import synth
+        self.m, self.n, self.k = m, n, k
+        self.blocks = synth.q4_0_blocks(n, k, seed=0)
+        self.X = synth.activations(m, k, seed=0)
+        wb = weight_bytes(n, k)
+        self.copies = max(min_copies, -(-2 * L2_BYTES // wb) + 1)
+        dev_blocks = torch.from_numpy(self.blocks.reshape(-1)).cuda()
+        base = torch.empty(q4lib.q4_0_packed_size(n, k), dtype=torch.uint8, device="cuda")
+        q4lib.q4_0_pack(base, dev_blocks, n, k)
+        self.W = [base] + [base.clone() for _ in range(self.copies - 1)]
+        del dev_blocks
+        self.Xd = torch.from_numpy(self.X).cuda()
+        self.Yd = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        self.ws, self.wsb = q4lib.workspace_for(m, k, n)
+        torch.cuda.synchronize()
+
+    def step(self, q4lib, i, stream):
+        q4lib.q4_0_matmul_ws(self.W[i % self.copies], self.Xd, self.Yd, self.m, self.k, self.n,
+                             self.ws, self.wsb, stream)
+
+
+def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None):
+    """Run `warmup` then time exactly `steps` steps as CUDA-graph replays.
+    Returns elapsed seconds of the timed steps."""
+    import torch
+    per_graph = max(1, min(per_graph, steps))
+    per_graph -= per_graph % wl.copies if per_graph >= wl.copies else 0
+    per_graph = max(per_graph, 1)
+
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(count):
+                    wl.step(q4lib, i, stream.cuda_stream)
+        return g
+
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 1)):
+            wl.step(q4lib, i, stream.cuda_stream)
+    torch.cuda.synchronize()
+    g_full = capture(per_graph)
+    rest = steps % per_graph
+    g_rest = capture(rest) if rest else None
+    with torch.cuda.stream(stream):
+        g_full.replay()
+    torch.cuda.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps // per_graph):
+            g_full.replay()
+        if g_rest is not None:
+            g_rest.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return start.elapsed_time(end) / 1e3, clocks
+
+
+def time_e2e(q4lib, wl, steps, stream):
+    """Public API with pinned host buffers: H2D of X, the call, D2H of Y."""
+    import torch
+    Xh = torch.from_numpy(wl.X).pin_memory()
+    Yh = torch.empty((wl.m, wl.n), dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            wl.Xd.copy_(Xh, non_blocking=True)
+            wl.step(q4lib, i, stream.cuda_stream)
+            Yh.copy_(wl.Yd, non_blocking=True)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            wl.Xd.copy_(Xh, non_blocking=True)
+            wl.step(q4lib, i, stream.cuda_stream)
+            Yh.copy_(wl.Yd, non_blocking=True)
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3, Xh.numel() * 4, Yh.numel() * 4
+
+
+def run_sweep(q4lib, stream, peaks):
+    import torch
+    out = []
+    for cfg in SWEEP:
+        m, n, k = cfg["m"], cfg["n"], cfg["k"]
+        wl = Workload(q4lib, m, n, k)
+        wb = weight_bytes(n, k)
+        est = wb / (peaks["hbm_gbs"] * 1e9) if m <= 16 else 2.0 * m * n * k / (peaks["bf16_tflops"] * 1e12)
+        steps = int(min(20000, max(200, 0.25 / max(est, 1e-7))))
+        steps -= steps % wl.copies
+        steps = max(steps, wl.copies)
+        sec, _ = time_graph(q4lib, wl, steps, 20, stream)
+        t = sec / steps
+        rec = dict(cfg, steps=steps, weight_copies=wl.copies, us_per_call=t * 1e6,
+                   weight_gbs=wb / t / 1e9, tokens_per_s=m / t)
+        if m <= 16:
+            rec["frac_hbm"] = rec["weight_gbs"] / peaks["hbm_gbs"]
+        else:
+            rec["tflops"] = 2.0 * m * n * k / t / 1e12
+            rec["frac_bf16"] = rec["tflops"] / peaks["bf16_tflops"]
+        out.append(rec)
+        del wl
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline(cfg, gpu_Y=None, tensor=False, seconds=10.0):
+    """Oracle throughput on the host cores (bounded sample), and, when the
+    GPU result is given, its max error over tolerance against the oracle."""
+    import oracle
+    from q4_quantized_linear_gb300 import synth
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    oracle.build()
+    blocks = synth.q4_0_blocks(n, k, seed=0)
+    X = synth.activations(m, k, seed=0)
+    # a bounded sample: leading rows of W, enough for about `seconds` of work
+    rows = n if m * n * k <= 2e9 else max(64, int(2e9 / (m * k)) // 64 * 64)
+    reps = 0
+    t0 = time.perf_counter()
+    Yr = B = None
+    while True:
+        Yr, B = oracle.matmul(blocks[:rows], X, rows, k)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    if tensor:
+        value, unit = reps * 2.0 * m * rows * k / el / 1e12, "TFLOP/s"
+    else:
+        value, unit = reps * weight_bytes(rows, k) / el / 1e9, "GB/s"
+    res = {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"{reps} oracle runs of m={m} x rows 0..{rows - 1} of n={n}, k={k} "
+                     f"({el:.1f} s, fp64, fixed order)"}
+    if gpu_Y is not None:
+        rtol, atol = (1e-3, 1e-5) if m <= 16 else (1e-2, 1e-4)
+        ratio = float((np.abs(gpu_Y[:, :rows].astype(np.float64) - Yr) / (rtol * B + atol)).max())
+        res["parity_max_err_over_tol"] = ratio
+    return res
+
+
+def native(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from q4_quantized_linear_gb300 import build
+    build.build()
+    from q4_quantized_linear_gb300 import binding as q4lib
+
+    peaks = load_peaks()
+    cfg = WORKLOADS[args.workload]
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    wb = weight_bytes(n, k)
+    flops = 2.0 * m * n * k
+    tensor = m > 16
+    stream = torch.cuda.Stream()
+    wl = Workload(q4lib, m, n, k)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sec, clocks = time_graph(q4lib, wl, args.steps, args.warmup, stream, sampler=sampler)
+    if world > 1:
+        t = torch.tensor([sec], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    unit = "TFLOP/s" if tensor else "GB/s"
+    per_step_units = flops / 1e12 if tensor else wb / 1e9
+    value = world * args.steps * per_step_units / sec
+    per_launch = sec / args.steps
+
+    e2e_steps = min(args.steps, 5000)
+    esec, h2d, d2h = time_e2e(q4lib, wl, e2e_steps, stream)
+    if world > 1:
+        t = torch.tensor([esec], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        esec = float(t.item())
+    e2e_value = world * e2e_steps * per_step_units / esec
+
+    gpu_Y = wl.Yd.cpu().numpy()
+    sweep = run_sweep(q4lib, stream, peaks) if (rank == 0 and not args.no_sweep) else None
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = None if args.no_cpu else cpu_baseline(cfg, gpu_Y, tensor)
+    achieved = per_step_units / per_launch
+    traffic = profiled_traffic(f"{args.workload}_m{m}_n{n}_k{k}")
+    if tensor:
+        peak, peak_key = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+    else:
+        peak, peak_key = peaks["hbm_gbs"], "hbm_gbs"
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": sec / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if tensor else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{cfg['name']}: Q4_0 W n={n} x k={k}, m={m}",
+            "m": m, "n": n, "k": k,
+            "weight_bytes_per_step": wb,
+            "flop_per_step": flops,
+            "l2": f"inputs larger than L2: {wl.copies} distinct packed weight copies "
+                  f"({wl.copies * wb / 1e6:.0f} MB) cycled step by step",
+            "launch": "CUDA graph replays of q4_0_matmul_ws, programmatic dependent launch",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor" if tensor else "hbm",
+            "kernel": "gemm_kernel (after xcast_kernel)" if tensor else f"decode_kernel<{1 if m <= 8 else 2}>",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": unit,
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json {peak_key})" if peaks["source"] == "measured"
+            else "fallback",
+            "units": ("algorithmic FLOP = 2*m*n*k per step (cast + GEMM launches)" if tensor
+                      else "algorithmic bytes = n*k/32*18 Q4_0 weight bytes per launch"),
+        },
+        "e2e": {"value": e2e_value, "unit": unit, "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (2 if tensor else 1),
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if sweep is not None:
+        line["sweep"] = sweep
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def reference(args):
+    """The oracle (CPU, as it stands) on the same config and metric."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    from q4_quantized_linear_gb300 import synth
+    oracle.build()
+    cfg = HEADLINE
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    wb = weight_bytes(n, k)
+    blocks = synth.q4_0_blocks(n, k, seed=0)
+    X = synth.activations(m, k, seed=0)
+    # each step is a bounded sample: a slice of rows sized so the run stays short
+    rows = min(n, 2048)
+    sample_bytes = weight_bytes(rows, k)
+    for _ in range(args.warmup):
+        oracle.matmul(blocks[:rows], X, rows, k)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul(blocks[:rows], X, rows, k)
+    el = time.perf_counter() - t0
+    value = args.steps * sample_bytes / el / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg['name']}: Q4_0 W n={n} x k={k}, m={m}", "m": m, "n": n, "k": k},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"each step: rows 0..{rows - 1} of W ({sample_bytes} weight bytes), m={m}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        if args.steps == 300000:
+            args.steps = 20
+        if args.warmup == 1000:
+            args.warmup = 3
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * q4mm.h -- C ABI of libq4mm, the GB300 (sm_103a) Q4_0 quantized linear layer.
+ *
+ * The operation (rembed "Architecture", section "The pluggable kernel
+ * interface": MatMul(dst, a, bT, m, k, n), C[m x n] = A[m x k] . B^T with
+ * B^T stored [n x k] row-major, an nn.Linear weight as stored):
+ *
+ *     Y[t][j] = sum_c X[t][c] * W[j][c]        t < m, j < n, c < k
+ *
+ * W is held as GGUF Q4_0 blocks (the format of the Q4_0 GGUF files the golem
+ * page runs, "Quickstart"): each block covers 32 consecutive weights of one
+ * row and is 18 bytes, an IEEE binary16 scale d (little endian) followed by
+ * qs[16]; byte i of qs holds weight i in its low nibble and weight i+16 in
+ * its high nibble (goinfer ch. 10, "Kernels and backends", section "Layout,
+ * concretely"); a weight is (q - 8) * d.
+ *
+ * One library call serves the three regimes the pages run the layer in:
+ * decode (m = 1), continuous batching where several slots' tokens share one
+ * read of the weights (golem, "Several conversations, one pass"; golem-server,
+ * "Several conversations, in one pass"), and prompt reading, where wide
+ * passes use tiled products ("Reading a prompt on the card": the mat-vec is
+ * built up to sixteen columns, tiled products take over from thirty-two).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named W_packed, blocks, X, Y, X_slots, Y_slots, slot_ids and
+ *     workspace are DEVICE pointers of the current CUDA device. The caller
+ *     owns and allocates every buffer; nothing is freed by the library.
+ *   - Work is enqueued on `stream` and the call returns without waiting.
+ *     Argument errors are returned synchronously before anything is enqueued.
+ *     A launch failure is returned as Q4_ERR_CUDA. A fault found by a kernel
+ *     while it runs (a bounded wait that ran out) is recorded in a per-device
+ *     status word that q4_last_device_status() reads once the stream has been
+ *     synchronised.
+ *   - There is no fallback: a device other than compute capability 10.3 is
+ *     refused with Q4_ERR_UNSUPPORTED_DEVICE.
+ *   - Results are bitwise identical from run to run for the same inputs and
+ *     sizes (no floating-point atomics; split sums are added in a fixed
+ *     order).
+ */
+#ifndef Q4MM_H
+#define Q4MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *q4mm_stream_t;
+
+#if defined(__GNUC__)
+#define Q4MM_API __attribute__((visibility("default")))
+#else
+#define Q4MM_API
+#endif
+
+/* Status codes. */
+#define Q4_OK 0
+#define Q4_ERR_INVALID_ARG 1        /* null pointer, k % 32 != 0, n <= 0, k <= 0, m < 0, bad ld */
+#define Q4_ERR_ALIGNMENT 2          /* a pointer or leading dimension breaks the alignment rule */
+#define Q4_ERR_UNSUPPORTED_DEVICE 3 /* current device is not compute capability 10.3 (GB300) */
+#define Q4_ERR_CUDA 4               /* a CUDA runtime call or kernel launch failed */
+#define Q4_ERR_DEVICE_TIMEOUT 5     /* a kernel's bounded wait ran out (read by q4_last_device_status) */
+#define Q4_ERR_WORKSPACE 6          /* workspace missing or smaller than q4_0_matmul_workspace_size() */
+#define Q4_ERR_NO_MEMORY 7          /* the library could not allocate its own workspace */
+
+/*
+ * Packed weight layout (what q4_0_pack writes). Repacking the blocks at load
+ * for the kernels' access order is the pages' layout step (goinfer ch. 10,
+ * "Making Go fast enough" and "Layout, concretely"; rembed "The pluggable
+ * kernel interface": a second, packed-weight interface). The payload is the
+ * same 18 bytes per block; only padding is added.
+ *
+ *   n is padded to a multiple of 64 rows, k to a multiple of 64 (a pair of
+ *   blocks). A record covers one tile of 16 rows x one pair of blocks and is
+ *   576 bytes:
+ *     bytes 0..63    32 fp16 scales; scale s = 4*g + 2*blk + h is d of row
+ *                    (tile start + g + 8*h), block (2*pair + blk), g < 8.
+ *     bytes 64..575  32 lanes x 16 bytes; lane L = 4*g + c holds the 4-byte
+ *                    words qs[4c..4c+3] of (row g, blk 0), (row g+8, blk 0),
+ *                    (row g, blk 1), (row g+8, blk 1), rows relative to the
+ *                    tile start.
+ *   Records are ordered [64-row group][pair][tile 0..3]: one group's data is
+ *   contiguous and one pair of a group is 2304 contiguous bytes.
+ *   Padding blocks have d = 0 and every nibble 8 (weight 0).
+ */
+
+/* Bytes of the packed form of an n x k Q4_0 matrix; 0 if n <= 0, k <= 0
+ * or k % 32 != 0. */
+Q4MM_API size_t q4_0_packed_size(int64_t n, int64_t k);
+
+/* Repack GGUF Q4_0 blocks into the packed layout (run once, at load).
+ *   W_packed: device, q4_0_packed_size(n, k) bytes, 16-byte aligned (written).
+ *   blocks:   device, n * (k/32) blocks of 18 bytes, row-major [n][k/32],
+ *             2-byte aligned (read).
+ *   n, k:     rows (output features) and columns (input features), k % 32 == 0.
+ * The two buffers must not overlap. Byte-exact: q4_0_unpack inverts it. */
+Q4MM_API int q4_0_pack(void *W_packed, const void *blocks, int64_t n, int64_t k,
+                       q4mm_stream_t stream);
+
+/* Inverse of q4_0_pack: write the n x (k/32) GGUF blocks back out.
+ *   blocks: device, n * (k/32) * 18 bytes, 2-byte aligned (written).
+ *   W_packed: device, as written by q4_0_pack for the same n, k (read). */
+Q4MM_API int q4_0_unpack(void *blocks, const void *W_packed, int64_t n, int64_t k,
+                         q4mm_stream_t stream);
+
+/* Bytes of device scratch q4_0_matmul_ws / q4_0_matmul_batched_slots_ws need
+ * for these sizes (0 when the call needs none). */
+Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
+
+/* Y[m x n] = X[m x k] . W^T, W given in packed form.
+ *   W_packed: device, packed by q4_0_pack for (n, k), 16-byte aligned.
+ *   X: device fp32 [m x k] row-major, 16-byte aligned.
+ *   Y: device fp32 [m x n] row-major, overwritten (no accumulate); 4-byte aligned.
+ *   m >= 0 (m == 0 does nothing), n >= 1, k >= 32, k % 32 == 0.
+ * Precision: for m <= 16 X is used at 16 significant bits (a two-term bf16
+ * split of each fp32 value) with exact integer weights, the block scale
+ * applied in fp32 and fp32 accumulation: |Y - Y_exact| <= 1e-3 * B + 1e-5
+ * with B = sum_c |X[t][c] * W[j][c]|. For m > 16 X is rounded to bf16
+ * (nearest even), weights to bf16 (nearest even of (q - 8) * d) and the
+ * tensor cores accumulate in fp32: |Y - Y_exact| <= 1e-2 * B + 1e-4.
+ * Scratch: this form uses a workspace the library allocates on the current
+ * device, once per (device, stream), grown when a call needs more. A call
+ * that has to grow it synchronises `stream` and is refused with
+ * Q4_ERR_WORKSPACE while the stream is being captured; make one call of the
+ * largest size before capturing. Use q4_0_matmul_ws to pass your own. */
+Q4MM_API int q4_0_matmul(const void *W_packed, const float *X, float *Y,
+                         int64_t m, int64_t k, int64_t n, q4mm_stream_t stream);
+
+/* As q4_0_matmul with caller-owned scratch: `workspace` (device, 256-byte
+ * aligned) of at least q4_0_matmul_workspace_size(m, k, n) bytes, which may be
+ * NULL when that size is 0. The library never allocates in this form.
+ * Zero a new workspace once before its first use (cudaMemset): its first
+ * 256 KB hold split-sum counters that every completed call leaves at zero, so
+ * one workspace serves calls of any shape in turn. After a call that ended in
+ * Q4_ERR_DEVICE_TIMEOUT, zero it again. Calls that can run at the same time
+ * need distinct workspaces. */
+Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
+                            int64_t m, int64_t k, int64_t n,
+                            void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
+
+/* Continuous batching: m active slots share one read of the weights.
+ * For i < m, row slot_ids[i] of X_slots produces row slot_ids[i] of Y_slots;
+ * every other row of Y_slots is left untouched. Equivalent to gathering the
+ * rows, q4_0_matmul, and scattering the results, with no extra copies.
+ *   X_slots: device fp32, row r at X_slots + r * ldx; ldx >= k, ldx % 4 == 0,
+ *            X_slots 16-byte aligned.
+ *   slot_ids: device int32[m], distinct, each in [0, number of slot rows).
+ *            Distinctness and range are the caller's contract (not checked on
+ *            the device; a repeated id makes the written row undefined).
+ *   Y_slots: device fp32, row r at Y_slots + r * ldy; ldy >= n.
+ * Same precision and scratch rules as q4_0_matmul. */
+Q4MM_API int q4_0_matmul_batched_slots(const void *W_packed, const float *X_slots, int64_t ldx,
+                                       const int32_t *slot_ids, int64_t m,
+                                       float *Y_slots, int64_t ldy,
+                                       int64_t k, int64_t n, q4mm_stream_t stream);
+
+/* As q4_0_matmul_batched_slots with caller-owned scratch (see q4_0_matmul_ws). */
+Q4MM_API int q4_0_matmul_batched_slots_ws(const void *W_packed, const float *X_slots, int64_t ldx,
+                                          const int32_t *slot_ids, int64_t m,
+                                          float *Y_slots, int64_t ldy,
+                                          int64_t k, int64_t n,
+                                          void *workspace, size_t workspace_bytes,
+                                          q4mm_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+Q4MM_API const char *q4_status_string(int status);
+
+/* Device status word of the current device: Q4_OK, or Q4_ERR_DEVICE_TIMEOUT
+ * if a kernel's bounded wait ran out since the word was last cleared.
+ * Synchronises the device. clear != 0 resets the word to Q4_OK. */
+Q4MM_API int q4_last_device_status(int clear);
+
+/* Limit, in nanoseconds, on each device-side wait of the library's kernels
+ * (default 2e9). Applies to launches made after the call, on every device. */
+Q4MM_API int q4_set_wait_limit_ns(uint64_t ns);
+
+/* Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing ever completes, for at most limit_ns nanoseconds, then
+ * records Q4_ERR_DEVICE_TIMEOUT in the device status word and returns. */
+Q4MM_API int q4_selftest_wait_timeout(uint64_t limit_ns, q4mm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4MM_H */

@@ -1,0 +1,202 @@
+"""Thin Python binding of libq4mm's C ABI (include/q4mm.h).
+
+Every function here has the name of the C entry point it calls and only
+marshals arguments (torch CUDA tensors or raw device addresses, the current
+torch stream by default); all arithmetic runs in libq4mm's CUDA kernels.
+There is no CPU path: if the library has not been built, importing this
+module raises.
+
+Build the library with ``python -m q4_quantized_linear_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB
+
+if not os.path.exists(LIB):
+    raise ImportError(
+        f"libq4mm is not built ({LIB} missing); run `python -m q4_quantized_linear_gb300.build`")
+
+_lib = ctypes.CDLL(LIB)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_INT = ctypes.c_int
+
+_SIGS = {
+    "q4_0_packed_size": (_SZ, [_I64, _I64]),
+    "q4_0_pack": (_INT, [_P, _P, _I64, _I64, _P]),
+    "q4_0_unpack": (_INT, [_P, _P, _I64, _I64, _P]),
+    "q4_0_matmul_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "q4_0_matmul": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "q4_0_matmul_ws": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "q4_0_matmul_batched_slots": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P]),
+    "q4_0_matmul_batched_slots_ws": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "q4_status_string": (ctypes.c_char_p, [_INT]),
+    "q4_last_device_status": (_INT, [_INT]),
+    "q4_set_wait_limit_ns": (_INT, [ctypes.c_uint64]),
+    "q4_selftest_wait_timeout": (_INT, [ctypes.c_uint64, _P]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+Q4_OK = 0
+Q4_ERR_INVALID_ARG = 1
+Q4_ERR_ALIGNMENT = 2
+Q4_ERR_UNSUPPORTED_DEVICE = 3
+Q4_ERR_CUDA = 4
+Q4_ERR_DEVICE_TIMEOUT = 5
+Q4_ERR_WORKSPACE = 6
+Q4_ERR_NO_MEMORY = 7
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {q4_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return LIB
+
+
+def exported_symbols() -> list[str]:
+    return sorted(_SIGS)
+
+
+def _addr(x) -> int | None:
+    """Device address of a torch tensor, or an int address as is (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != Q4_OK:
+        raise Q4Error(rc, where)
+    return rc
+
+
+# ------------------------------------------------------------- C ABI calls --
+
+def q4_status_string(status: int) -> str:
+    return _lib.q4_status_string(int(status)).decode()
+
+
+def q4_0_packed_size(n: int, k: int) -> int:
+    return int(_lib.q4_0_packed_size(n, k))
+
+
+def q4_0_matmul_workspace_size(m: int, k: int, n: int) -> int:
+    return int(_lib.q4_0_matmul_workspace_size(m, k, n))
+
+
+def q4_0_pack(W_packed, blocks, n: int, k: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_pack(_addr(W_packed), _addr(blocks), n, k, _stream(stream))
+    return _check(rc, "q4_0_pack") if check else rc
+
+
+def q4_0_unpack(blocks, W_packed, n: int, k: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_unpack(_addr(blocks), _addr(W_packed), n, k, _stream(stream))
+    return _check(rc, "q4_0_unpack") if check else rc
+
+
+def q4_0_matmul(W_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_matmul(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _stream(stream))
+    return _check(rc, "q4_0_matmul") if check else rc
+
+
+def q4_0_matmul_ws(W_packed, X, Y, m: int, k: int, n: int, workspace, workspace_bytes: int,
+                   stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_matmul_ws(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _addr(workspace),
+                             workspace_bytes, _stream(stream))
+    return _check(rc, "q4_0_matmul_ws") if check else rc
+
+
+def q4_0_matmul_batched_slots(W_packed, X_slots, ldx: int, slot_ids, m: int, Y_slots, ldy: int,
+                              k: int, n: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_matmul_batched_slots(_addr(W_packed), _addr(X_slots), ldx, _addr(slot_ids), m,
+                                        _addr(Y_slots), ldy, k, n, _stream(stream))
+    return _check(rc, "q4_0_matmul_batched_slots") if check else rc
+
+
+def q4_0_matmul_batched_slots_ws(W_packed, X_slots, ldx: int, slot_ids, m: int, Y_slots, ldy: int,
+                                 k: int, n: int, workspace, workspace_bytes: int, stream=None,
+                                 check: bool = True) -> int:
+    rc = _lib.q4_0_matmul_batched_slots_ws(_addr(W_packed), _addr(X_slots), ldx, _addr(slot_ids), m,
+                                           _addr(Y_slots), ldy, k, n, _addr(workspace),
+                                           workspace_bytes, _stream(stream))
+    return _check(rc, "q4_0_matmul_batched_slots_ws") if check else rc
+
+
+def q4_last_device_status(clear: bool = True) -> int:
+    return int(_lib.q4_last_device_status(1 if clear else 0))
+
+
+def q4_set_wait_limit_ns(ns: int) -> int:
+    return _check(_lib.q4_set_wait_limit_ns(int(ns)), "q4_set_wait_limit_ns")
+
+
+def q4_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return _check(_lib.q4_selftest_wait_timeout(int(limit_ns), _stream(stream)), "q4_selftest_wait_timeout")
+
+
+# ------------------------------------------------------ tensor conveniences --
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def workspace_for(m: int, k: int, n: int, device=None, stream=None):
+    """A zeroed torch uint8 workspace large enough for (m, k, n), cached per
+    (device, stream) and grown on demand (torch's allocator, no cudaMalloc
+    per call once warm). Returns (tensor or None, bytes)."""
+    import torch
+    need = q4_0_matmul_workspace_size(m, k, n)
+    if need == 0:
+        return None, 0
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = (dev.index, _stream(stream))
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < need:
+            buf = torch.zeros(max(need, 1 << 20), dtype=torch.uint8, device=dev)
+            _ws_cache[key] = buf
+    return buf, buf.numel()
+
+
+def pack(blocks, n: int, k: int, stream=None):
+    """GGUF Q4_0 blocks (torch uint8 CUDA tensor, n*(k/32)*18 bytes) -> packed tensor."""
+    import torch
+    out = torch.empty(q4_0_packed_size(n, k), dtype=torch.uint8, device=blocks.device)
+    q4_0_pack(out, blocks, n, k, stream)
+    return out
+
+
+def matmul(W_packed, X, n: int, out=None, stream=None):
+    """Y = X . W^T for fp32 CUDA X [m x k]; returns Y [m x n] fp32."""
+    import torch
+    m, k = X.shape
+    Y = torch.empty((m, n), dtype=torch.float32, device=X.device) if out is None else out
+    ws, wsb = workspace_for(m, k, n, X.device, stream)
+    q4_0_matmul_ws(W_packed, X, Y, m, k, n, ws, wsb, stream)
+    return Y

@@ -1,0 +1,408 @@
+// q4mm_api.cu -- the C ABI of libq4mm (declared in include/q4mm.h): argument
+// validation, per-device state, workspace handling and dispatch between the
+// decode kernel (m <= 16) and the tensor-core prefill kernels (m > 16).
+//
+// The dispatch point follows golem, "Reading a prompt on the card": the
+// mat-vec is built up to sixteen columns and tiled products take over beyond.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/q4mm.h"
+#include "q4mm_internal.h"
+
+namespace q4 {
+
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDecodeMaxM = 16;
+
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+
+struct DeviceSlot {
+    std::once_flag once;
+    int rc = Q4_OK;
+    DeviceInfo info;
+};
+DeviceSlot g_dev[kMaxDevices];
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+// Current device, checked to be a GB300-class part (compute capability 10.3).
+int current_device(DeviceInfo *out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return Q4_ERR_CUDA;
+    }
+    DeviceSlot &slot = g_dev[dev];
+    std::call_once(slot.once, [&] {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            slot.rc = Q4_ERR_CUDA;
+            return;
+        }
+        if (major != 10 || minor != 3) {
+            slot.rc = Q4_ERR_UNSUPPORTED_DEVICE;
+            return;
+        }
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            slot.rc = Q4_ERR_CUDA;
+            return;
+        }
+        slot.info.device = dev;
+        slot.info.sm_count = sms;
+        slot.info.status = static_cast<int *>(addr);
+        slot.rc = Q4_OK;
+    });
+    if (slot.rc == Q4_OK) *out = slot.info;
+    return slot.rc;
+}
+
+int map_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return Q4_OK;
+    cudaGetLastError();
+    return Q4_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_nk(int64_t n, int64_t k)
+{
+    return n >= 1 && k >= 32 && (k % 32) == 0 && n <= (int64_t(1) << 31) - 64 && k <= (int64_t(1) << 24);
+}
+
+// Library-owned scratch for the forms without a workspace argument: one
+// buffer per (device, stream), zeroed when created, grown on demand.
+int library_workspace(int dev, cudaStream_t s, size_t need, void **out)
+{
+    *out = nullptr;
+    if (need == 0) return Q4_OK;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace &w = g_ws[{dev, s}];
+    if (w.bytes >= need) {
+        *out = w.ptr;
+        return Q4_OK;
+    }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return Q4_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return Q4_ERR_WORKSPACE;
+    if (w.ptr) {
+        if (cudaStreamSynchronize(s) != cudaSuccess || cudaFree(w.ptr) != cudaSuccess) {
+            cudaGetLastError();
+            return Q4_ERR_CUDA;
+        }
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    const size_t bytes = static_cast<size_t>(round_up(static_cast<int64_t>(need), 1 << 20));
+    if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        w.ptr = nullptr;
+        return Q4_ERR_NO_MEMORY;
+    }
+    if (cudaMemsetAsync(w.ptr, 0, bytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return Q4_ERR_CUDA;
+    }
+    w.bytes = bytes;
+    *out = w.ptr;
+    return Q4_OK;
+}
+
+size_t workspace_size(int64_t m, int64_t k, int64_t n, int sm_count)
+{
+    if (m <= 0) return 0;
+    if (m <= kDecodeMaxM) {
+        DecodePlan p;
+        return plan_decode(m, k, n, sm_count, &p) ? p.ws_bytes : 0;
+    }
+    PrefillPlan p;
+    return plan_prefill(m, k, n, sm_count, &p) ? p.ws_bytes : 0;
+}
+
+// Shared body of every matmul entry point. rows == nullptr: plain X/Y rows.
+int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows, float *Y, int64_t ldy,
+                int64_t m, int64_t k, int64_t n, void *workspace, size_t ws_bytes, bool library_ws, cudaStream_t s)
+{
+    if (!W || !X || !Y || m < 0 || !valid_nk(n, k) || ldx < k || ldy < n) return Q4_ERR_INVALID_ARG;
+    if (m > (int64_t(1) << 24)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(X, 16) || (ldx % 4) != 0 || !aligned(Y, 4)) return Q4_ERR_ALIGNMENT;
+    if (workspace && !aligned(workspace, 256)) return Q4_ERR_ALIGNMENT;
+    if (m == 0) return Q4_OK;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    const uint64_t wait_ns = g_wait_ns.load();
+
+    if (m <= kDecodeMaxM) {
+        DecodePlan plan;
+        if (!plan_decode(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
+        if (library_ws) {
+            rc = library_workspace(dev.device, s, plan.ws_bytes, &workspace);
+            if (rc != Q4_OK) return rc;
+            ws_bytes = plan.ws_bytes;
+        }
+        if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes)) return Q4_ERR_WORKSPACE;
+        DecodeArgs a{};
+        a.W = static_cast<const uint8_t *>(W);
+        a.X = X;
+        a.rows = rows;
+        a.ldx = ldx;
+        a.Y = Y;
+        a.ldy = ldy;
+        a.partials = plan.ws_bytes ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.ws_partials_off)
+                                   : nullptr;
+        a.counters = plan.ws_bytes
+                         ? reinterpret_cast<unsigned *>(static_cast<uint8_t *>(workspace) + plan.ws_counters_off)
+                         : nullptr;
+        a.status = dev.status;
+        a.wait_ns = wait_ns;
+        a.m = static_cast<int>(m);
+        a.n = static_cast<int>(n);
+        a.nb = static_cast<int>(k / 32);
+        a.np = static_cast<int>(ceil_div(k, kPairK));
+        a.groups = static_cast<int>(ceil_div(n, kGroupRows));
+        a.S = plan.S;
+        a.pbase = plan.pbase;
+        a.prem = plan.prem;
+        a.stages = plan.stages;
+        a.xs_bytes = plan.xs_bytes;
+        return map_cuda(launch_decode(plan, a, s));
+    }
+
+    PrefillPlan plan;
+    if (!plan_prefill(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
+    if (library_ws) {
+        rc = library_workspace(dev.device, s, plan.ws_bytes, &workspace);
+        if (rc != Q4_OK) return rc;
+        ws_bytes = plan.ws_bytes;
+    }
+    if (!workspace || ws_bytes < plan.ws_bytes) return Q4_ERR_WORKSPACE;
+    XcastArgs xa{};
+    xa.X = X;
+    xa.rows = rows;
+    xa.ldx = ldx;
+    xa.ximg = static_cast<uint8_t *>(workspace) + plan.ws_ximg_off;
+    xa.m = static_cast<int>(m);
+    xa.nb = static_cast<int>(k / 32);
+    xa.np = static_cast<int>(ceil_div(k, kPairK));
+    xa.T = plan.T;
+    xa.ts = plan.ts;
+    PrefillArgs pa{};
+    pa.W = static_cast<const uint8_t *>(W);
+    pa.ximg = static_cast<const uint8_t *>(workspace) + plan.ws_ximg_off;
+    pa.Y = Y;
+    pa.rows = rows;
+    pa.ldy = ldy;
+    pa.status = dev.status;
+    pa.wait_ns = wait_ns;
+    pa.m = static_cast<int>(m);
+    pa.n = static_cast<int>(n);
+    pa.np = xa.np;
+    pa.groups = static_cast<int>(ceil_div(n, kGroupRows));
+    pa.T = plan.T;
+    pa.ts = plan.ts;
+    pa.rb = plan.rb;
+    pa.ra = plan.ra;
+    pa.rw = plan.rw;
+    pa.tmem_cols = plan.tmem_cols;
+    return map_cuda(launch_prefill(plan, xa, pa, s));
+}
+
+} // namespace
+
+cudaError_t set_max_smem(const void *func, size_t bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({dev, func});
+    if (it == done.end()) {
+        // the dynamic limit plus the kernel's static shared memory may not
+        // exceed the device's per-block opt-in maximum
+        int optin = 0;
+        cudaFuncAttributes fa{};
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, func);
+        if (e != cudaSuccess) return e;
+        const size_t limit = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(limit));
+        if (e != cudaSuccess) return e;
+        it = done.emplace(std::make_pair(dev, func), limit).first;
+    }
+    return bytes <= it->second ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void **args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+} // namespace q4
+
+using namespace q4;
+
+extern "C" {
+
+Q4MM_API size_t q4_0_packed_size(int64_t n, int64_t k)
+{
+    if (!valid_nk(n, k)) return 0;
+    return static_cast<size_t>(ceil_div(n, kGroupRows) * ceil_div(k, kPairK) * kPairBytes);
+}
+
+Q4MM_API int q4_0_pack(void *W_packed, const void *blocks, int64_t n, int64_t k, q4mm_stream_t stream)
+{
+    if (!W_packed || !blocks || !valid_nk(n, k)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W_packed, 16) || !aligned(blocks, 2)) return Q4_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    return map_cuda(launch_pack(static_cast<uint8_t *>(W_packed), static_cast<const uint8_t *>(blocks), n, k,
+                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+Q4MM_API int q4_0_unpack(void *blocks, const void *W_packed, int64_t n, int64_t k, q4mm_stream_t stream)
+{
+    if (!W_packed || !blocks || !valid_nk(n, k)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W_packed, 16) || !aligned(blocks, 2)) return Q4_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    return map_cuda(launch_unpack(static_cast<uint8_t *>(blocks), static_cast<const uint8_t *>(W_packed), n, k,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n)
+{
+    if (m <= 0 || !valid_nk(n, k)) return 0;
+    DeviceInfo dev;
+    if (current_device(&dev) != Q4_OK) return 0;
+    return workspace_size(m, k, n, dev.sm_count);
+}
+
+Q4MM_API int q4_0_matmul(const void *W_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,
+                         q4mm_stream_t stream)
+{
+    return matmul_impl(W_packed, X, k, nullptr, Y, n, m, k, n, nullptr, 0, true,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,
+                            void *workspace, size_t workspace_bytes, q4mm_stream_t stream)
+{
+    return matmul_impl(W_packed, X, k, nullptr, Y, n, m, k, n, workspace, workspace_bytes, false,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+Q4MM_API int q4_0_matmul_batched_slots(const void *W_packed, const float *X_slots, int64_t ldx,
+                                       const int32_t *slot_ids, int64_t m, float *Y_slots, int64_t ldy, int64_t k,
+                                       int64_t n, q4mm_stream_t stream)
+{
+    if (m > 0 && !slot_ids) return Q4_ERR_INVALID_ARG;
+    if (slot_ids && !aligned(slot_ids, 4)) return Q4_ERR_ALIGNMENT;
+    return matmul_impl(W_packed, X_slots, ldx, slot_ids, Y_slots, ldy, m, k, n, nullptr, 0, true,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+Q4MM_API int q4_0_matmul_batched_slots_ws(const void *W_packed, const float *X_slots, int64_t ldx,
+                                          const int32_t *slot_ids, int64_t m, float *Y_slots, int64_t ldy, int64_t k,
+                                          int64_t n, void *workspace, size_t workspace_bytes, q4mm_stream_t stream)
+{
+    if (m > 0 && !slot_ids) return Q4_ERR_INVALID_ARG;
+    if (slot_ids && !aligned(slot_ids, 4)) return Q4_ERR_ALIGNMENT;
+    return matmul_impl(W_packed, X_slots, ldx, slot_ids, Y_slots, ldy, m, k, n, workspace, workspace_bytes, false,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+Q4MM_API const char *q4_status_string(int status)
+{
+    switch (status) {
+    case Q4_OK: return "ok";
+    case Q4_ERR_INVALID_ARG: return "invalid argument";
+    case Q4_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case Q4_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case Q4_ERR_CUDA: return "CUDA runtime error";
+    case Q4_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
+    case Q4_ERR_WORKSPACE: return "workspace missing or too small";
+    case Q4_ERR_NO_MEMORY: return "out of device memory";
+    default: return "unknown status";
+    }
+}
+
+Q4MM_API int q4_last_device_status(int clear)
+{
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return Q4_ERR_CUDA;
+    }
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return Q4_ERR_CUDA;
+    }
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return Q4_ERR_CUDA;
+        }
+    }
+    return v;
+}
+
+Q4MM_API int q4_set_wait_limit_ns(uint64_t ns)
+{
+    if (ns == 0) return Q4_ERR_INVALID_ARG;
+    g_wait_ns.store(ns);
+    return Q4_OK;
+}
+
+Q4MM_API int q4_selftest_wait_timeout(uint64_t limit_ns, q4mm_stream_t stream)
+{
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return Q4_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    return map_cuda(launch_wait_selftest(dev.status, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+} // extern "C"

@@ -17,3 +17,16 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+TESTS = os.path.dirname(os.path.abspath(__file__))
+if TESTS not in sys.path:
+    sys.path.insert(0, TESTS)
+
+
+@pytest.fixture(scope="session")
+def q4lib():
+    """The built libq4mm binding (builds in-tree if needed)."""
+    from q4_quantized_linear_gb300 import build
+    build.build()
+    from q4_quantized_linear_gb300 import binding
+    return binding

@@ -1,0 +1,234 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Covers the repacker (byte-exact), decode m = 1..16 and prefill m > 16 on
+ragged shapes spanning several tiles, the workload sizes (full compare
+where the oracle finishes in seconds, sampled elements otherwise),
+continuous batching through slot indices, and the degenerate cases: m = 0,
+all-zero weights, exact integer inputs (bit-exact), NaN/Inf propagation,
+zero and negative scales, run-to-run bitwise determinism, and the bounded
+device wait.
+"""
+
+import numpy as np
+import pytest
+
+from q4_quantized_linear_gb300 import synth
+from q4_testlib import assert_parity, pack_dev, run_matmul, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+# ------------------------------------------------------------- repacker ----
+
+@pytest.mark.parametrize("n,k", [(1, 32), (16, 64), (64, 64), (70, 96), (333, 1056), (9728, 2560)])
+def test_pack_matches_oracle_layout_and_unpack_inverts(q4lib, oracle_mod, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=n + k)
+    W = pack_dev(q4lib, blocks, n, k)
+    torch.cuda.synchronize()
+    ref = oracle_mod.pack_reference(blocks, n, k)
+    assert np.array_equal(W.cpu().numpy(), ref), "packed bytes differ from the layout reference"
+    back = torch.empty(blocks.size, dtype=torch.uint8, device="cuda")
+    q4lib.q4_0_unpack(back, W, n, k)
+    torch.cuda.synchronize()
+    assert np.array_equal(back.cpu().numpy(), blocks.reshape(-1)), "unpack(pack(W)) != W"
+
+
+# --------------------------------------------------------- small shapes ----
+
+SHAPES = [(1, 32), (64, 64), (65, 96), (200, 1056), (1000, 2080), (333, 4096), (130, 8192 + 64)]
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8, 9, 13, 16])
+@pytest.mark.parametrize("n,k", SHAPES)
+def test_decode_parity(q4lib, oracle_mod, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=1000 + n)
+    X = synth.activations(m, k, seed=2000 + m)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, f"decode m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("m", [17, 31, 64, 100, 257, 300])
+@pytest.mark.parametrize("n,k", [(64, 64), (65, 96), (200, 1056), (513, 2080), (260, 640)])
+def test_prefill_parity(q4lib, oracle_mod, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=3000 + n)
+    X = synth.activations(m, k, seed=4000 + m)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, f"prefill m={m} n={n} k={k}")
+
+
+def test_library_workspace_forms(q4lib, oracle_mod):
+    for (m, n, k) in [(4, 2560, 9728), (40, 300, 1024), (1, 500, 256)]:
+        blocks = synth.q4_0_blocks(n, k, seed=5)
+        X = synth.activations(m, k, seed=6)
+        W = pack_dev(q4lib, blocks, n, k)
+        Y = run_matmul(q4lib, W, X, n, use_library_ws=True)
+        Yr, B = oracle_mod.matmul(blocks, X, n, k)
+        assert_parity(Y, Yr, B, m, f"library workspace m={m}")
+
+
+# ----------------------------------------------------- workload sizes ----
+
+FULL = [  # (m, n, k): oracle compares every element
+    (1, 1024, 1024),     # single GEMV
+    (1, 9728, 2560),     # decode up-projection
+    (4, 9728, 2560),     # 4 slots, up-projection
+    (4, 2560, 9728),     # 4 slots, down-projection (K split)
+    (1, 14336, 4096), (2, 14336, 4096), (4, 14336, 4096), (8, 14336, 4096), (16, 14336, 4096),
+]
+
+
+@pytest.mark.parametrize("m,n,k", FULL)
+def test_workload_sizes_full_compare(q4lib, oracle_mod, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=0)
+    X = synth.activations(m, k, seed=0)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, f"m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(4, 151936, 2560), (540, 9728, 2560)])
+def test_workload_sizes_sampled(q4lib, oracle_mod, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=0)
+    X = synth.activations(m, k, seed=0)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    r = np.random.default_rng(7)
+    cnt = 6000
+    t = r.integers(0, m, cnt)
+    j = r.integers(0, n, cnt)
+    # always include the corners and the last row/column
+    t = np.concatenate([t, [0, m - 1, 0, m - 1]])
+    j = np.concatenate([j, [0, 0, n - 1, n - 1]])
+    Yr, B = oracle_mod.matmul_sampled(blocks, X, n, k, t, j)
+    assert_parity(Y[t, j], Yr, B, m, f"sampled m={m} n={n} k={k}")
+
+
+# ------------------------------------------------- continuous batching ----
+
+@pytest.mark.parametrize("m,slots,n,k", [(1, 8, 300, 512), (4, 40, 9728, 2560), (16, 20, 200, 4096),
+                                         (4, 12, 2560, 9728), (20, 64, 260, 1024), (37, 40, 130, 640)])
+def test_batched_slots(q4lib, oracle_mod, m, slots, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=11)
+    ldx, ldy = k + 8, n + 5
+    Xs = np.zeros((slots, ldx), dtype=np.float32)
+    Xs[:, :k] = synth.activations(slots, k, seed=12)
+    ids = synth.slot_ids(m, slots, seed=13)
+    W = pack_dev(q4lib, blocks, n, k)
+    Xd = to_dev(Xs)
+    sentinel = np.float32(-12345.5)
+    Yd = torch.full((slots, ldy), float(sentinel), dtype=torch.float32, device="cuda")
+    idd = to_dev(ids)
+    ws, wsb = q4lib.workspace_for(m, k, n)
+    q4lib.q4_0_matmul_batched_slots_ws(W, Xd, ldx, idd, m, Yd, ldy, k, n, ws, wsb)
+    torch.cuda.synchronize()
+    assert q4lib.q4_last_device_status() == 0
+    Y = Yd.cpu().numpy()
+    Yr, B = oracle_mod.matmul(blocks, Xs[ids, :k], n, k)
+    assert_parity(Y[ids, :n], Yr, B, m, f"slots m={m}")
+    untouched = np.ones(slots, dtype=bool)
+    untouched[ids] = False
+    assert np.all(Y[untouched] == sentinel), "rows of inactive slots were written"
+    assert np.all(Y[ids, n:] == sentinel), "padding columns of active rows were written"
+
+
+# ------------------------------------------------------ degenerate cases ----
+
+def test_m_zero_is_a_no_op(q4lib):
+    n, k = 64, 64
+    W = pack_dev(q4lib, synth.q4_0_blocks(n, k), n, k)
+    X = torch.zeros((1, k), dtype=torch.float32, device="cuda")
+    Y = torch.full((1, n), 3.0, dtype=torch.float32, device="cuda")
+    q4lib.q4_0_matmul(W, X, Y, 0, k, n)
+    torch.cuda.synchronize()
+    assert torch.all(Y == 3.0)
+
+
+@pytest.mark.parametrize("m", [1, 7, 16, 17, 100])
+def test_all_eights_give_exact_zero(q4lib, m):
+    n, k = 130, 640
+    blocks = synth.q4_0_blocks(n, k, seed=21)
+    blocks[:, :, 2:] = 0x88
+    X = synth.activations(m, k, seed=22)
+    Y = run_matmul(q4lib, pack_dev(q4lib, blocks, n, k), X, n)
+    assert np.all(Y == 0.0)
+
+
+@pytest.mark.parametrize("m", [1, 5, 16, 17, 64, 300])
+def test_exact_integer_case_is_bit_exact(q4lib, oracle_mod, m):
+    """Power-of-two scales and small integer X: every partial sum is an exact
+    integer times a power of two, on both paths, so the results are equal."""
+    n, k = 200, 1024
+    blocks = synth.q4_0_blocks(n, k, seed=31)
+    nb = k // 32
+    e = (synth.draw_u64(31, 9, n * nb) % np.uint64(6)).astype(np.int64) - 8
+    d = np.ldexp(1.0, e).astype(np.float16).reshape(n, nb)
+    blocks[:, :, 0:2] = d.astype("<f2").view(np.uint8).reshape(n, nb, 2)
+    xi = (synth.draw_u64(32, 9, m * k) % np.uint64(33)).astype(np.int64) - 16
+    X = xi.astype(np.float32).reshape(m, k)
+    Y = run_matmul(q4lib, pack_dev(q4lib, blocks, n, k), X, n)
+    Yr, _ = oracle_mod.matmul(blocks, X, n, k)
+    assert np.array_equal(Y.astype(np.float64), Yr)
+
+
+@pytest.mark.parametrize("m", [1, 16, 17, 64])
+def test_nonfinite_x_propagates(q4lib, oracle_mod, m):
+    n, k = 100, 256
+    blocks = synth.q4_0_blocks(n, k, seed=41)
+    X = synth.activations(m, k, seed=42)
+    X[0, 5] = np.nan
+    if m > 1:
+        X[m - 1, 77] = np.inf
+    Y = run_matmul(q4lib, pack_dev(q4lib, blocks, n, k), X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, "non-finite X")
+
+
+@pytest.mark.parametrize("m", [3, 33])
+def test_zero_and_negative_scales(q4lib, oracle_mod, m):
+    n, k = 96, 512
+    blocks = synth.q4_0_blocks(n, k, seed=51)
+    blocks[::3, ::2, 0:2] = 0                       # d = +0
+    blocks[1::3, :, 1] |= 0x80                      # d negative
+    X = synth.activations(m, k, seed=52)
+    Y = run_matmul(q4lib, pack_dev(q4lib, blocks, n, k), X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, "zero/negative scales")
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (16, 14336, 4096), (540, 9728, 2560)])
+def test_bitwise_deterministic(q4lib, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=61)
+    X = synth.activations(m, k, seed=62)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y1 = run_matmul(q4lib, W, X, n)
+    Y2 = run_matmul(q4lib, W, X, n)
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(q4lib, oracle_mod):
+    import time
+    q4lib.q4_last_device_status(clear=True)
+    t0 = time.time()
+    q4lib.q4_selftest_wait_timeout(5_000_000)       # 5 ms
+    assert q4lib.q4_last_device_status(clear=True) == q4lib.Q4_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 5.0
+    # the context still works
+    n, k, m = 64, 128, 2
+    blocks = synth.q4_0_blocks(n, k, seed=71)
+    X = synth.activations(m, k, seed=72)
+    Y = run_matmul(q4lib, pack_dev(q4lib, blocks, n, k), X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, "after timeout")
