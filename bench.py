@@ -338,6 +338,10 @@ def native(args):
     build.build()
     from q4_quantized_linear_gb300 import binding as q4lib
 
+    # the packed weights are written once, before any timing, and then only
+    # read: declare them read-only so consecutive calls overlap their weight
+    # streams (programmatic dependent launch)
+    q4lib.q4_set_weight_prefetch(True)
     peaks = load_peaks()
     cfg = WORKLOADS[args.workload]
     m, n, k = cfg["m"], cfg["n"], cfg["k"]
@@ -405,7 +409,8 @@ def native(args):
             "flop_per_step": flops,
             "l2": f"inputs larger than L2: {wl.copies} distinct packed weight copies "
                   f"({wl.copies * wb / 1e6:.0f} MB) cycled step by step",
-            "launch": "CUDA graph replays of q4_0_matmul_ws, programmatic dependent launch",
+            "launch": "CUDA graph replays of q4_0_matmul_ws, programmatic dependent launch, "
+                      "weights declared read-only (q4_set_weight_prefetch)",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {

@@ -120,8 +120,9 @@ Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
  * split of each fp32 value) with exact integer weights, the block scale
  * applied in fp32 and fp32 accumulation: |Y - Y_exact| <= 1e-3 * B + 1e-5
  * with B = sum_c |X[t][c] * W[j][c]|. For m > 16 X is rounded to bf16
- * (nearest even), weights to bf16 (nearest even of (q - 8) * d) and the
- * tensor cores accumulate in fp32: |Y - Y_exact| <= 1e-2 * B + 1e-4.
+ * (nearest even), each weight is the exact (q - 8) times d rounded to bf16,
+ * rounded to bf16 (relative error <= 2^-8), and the tensor cores accumulate
+ * in fp32: |Y - Y_exact| <= 1e-2 * B + 1e-4.
  * Scratch: this form uses a workspace the library allocates on the current
  * device, once per (device, stream), grown when a call needs more. A call
  * that has to grow it synchronises `stream` and is refused with
@@ -177,6 +178,17 @@ Q4MM_API int q4_last_device_status(int clear);
 /* Limit, in nanoseconds, on each device-side wait of the library's kernels
  * (default 2e9). Applies to launches made after the call, on every device. */
 Q4MM_API int q4_set_wait_limit_ns(uint64_t ns);
+
+/* Declare packed weights read-only while matmuls run (default: not declared).
+ * When enabled, a decode-path kernel (m <= 16) starts streaming W_packed
+ * before the kernel that precedes it in the stream has finished, overlapping
+ * the two (programmatic dependent launch); X, Y and the workspace are still
+ * read only after that kernel completes. Enable it only if no kernel writes a
+ * W_packed immediately before a matmul that reads it in the same stream
+ * (after q4_0_pack, synchronise or record an event before the first matmul).
+ * The prefill path always overlaps its weight reads: the kernel before its
+ * GEMM is its own X cast. Applies to launches made after the call. */
+Q4MM_API int q4_set_weight_prefetch(int enable);
 
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * barrier nothing ever completes, for at most limit_ns nanoseconds, then

@@ -41,6 +41,7 @@ _SIGS = {
     "q4_status_string": (ctypes.c_char_p, [_INT]),
     "q4_last_device_status": (_INT, [_INT]),
     "q4_set_wait_limit_ns": (_INT, [ctypes.c_uint64]),
+    "q4_set_weight_prefetch": (_INT, [_INT]),
     "q4_selftest_wait_timeout": (_INT, [ctypes.c_uint64, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -154,6 +155,10 @@ def q4_last_device_status(clear: bool = True) -> int:
 
 def q4_set_wait_limit_ns(ns: int) -> int:
     return _check(_lib.q4_set_wait_limit_ns(int(ns)), "q4_set_wait_limit_ns")
+
+
+def q4_set_weight_prefetch(enable: bool) -> int:
+    return _check(_lib.q4_set_weight_prefetch(1 if enable else 0), "q4_set_weight_prefetch")
 
 
 def q4_selftest_wait_timeout(limit_ns: int, stream=None) -> int:

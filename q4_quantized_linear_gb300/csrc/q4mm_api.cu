@@ -25,6 +25,7 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kDecodeMaxM = 16;
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
+std::atomic<int> g_prefetch_w{0};
 
 struct DeviceSlot {
     std::once_flag once;
@@ -190,6 +191,7 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.prem = plan.prem;
         a.stages = plan.stages;
         a.xs_bytes = plan.xs_bytes;
+        a.prefetch_w = g_prefetch_w.load();
         return map_cuda(launch_decode(plan, a, s));
     }
 
@@ -393,6 +395,12 @@ Q4MM_API int q4_set_wait_limit_ns(uint64_t ns)
 {
     if (ns == 0) return Q4_ERR_INVALID_ARG;
     g_wait_ns.store(ns);
+    return Q4_OK;
+}
+
+Q4MM_API int q4_set_weight_prefetch(int enable)
+{
+    g_prefetch_w.store(enable ? 1 : 0);
     return Q4_OK;
 }
 

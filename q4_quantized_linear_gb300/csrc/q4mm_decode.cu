@@ -7,7 +7,7 @@
 // calls the quantised GEMV the decode workhorse.
 //
 // Design (GB300, one kernel per call):
-//   * Persistent CTAs of 8 warps (two per SM sub-partition). CTA c owns a K
+//   * Persistent CTAs of 16 warps (8 when m > 8). CTA c owns a K
 //     slice (when one is needed) and a strided set of 64-row groups. Each
 //     warp streams its own share of every group's pairs (2304 contiguous
 //     bytes per pair) through a private ring of shared-memory stages filled
@@ -24,7 +24,7 @@
 //     partial sum, which is scaled by the block's fp16 d in fp32 and
 //     accumulated. Tensor cores here only replace CUDA-core FMAs: the kernel
 //     stays bound by the weight bytes.
-//   * The 8 warps' partials of a group are added in a fixed order through
+//   * The warps' partials of a group are added in a fixed order through
 //     shared memory. With K slices, each slice writes its partial to the
 //     workspace and the last slice to finish (a counter) adds all slices in
 //     slice order, so results are bitwise reproducible.
@@ -37,14 +37,16 @@
 namespace q4 {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = 256;
 constexpr int kErrTimeout = 5; // Q4_ERR_DEVICE_TIMEOUT
-constexpr int kStageUnroll = 8; // X items whose loads are in flight together
+constexpr int kStageUnroll = 4; // X items whose loads are in flight together
+
+// Warps per CTA: 16 (four per SM sub-partition, at most 128 registers) for
+// one n-tile; 8 for two n-tiles, whose accumulators need more registers.
+__host__ __device__ constexpr int warps_for(int NT) { return NT == 1 ? 16 : 8; }
 
 // Shared-memory bytes of the X region per pair: NT x 2 blocks x (hi, lo) x 512.
 __host__ __device__ constexpr int xs_pair_bytes(int NT) { return NT * 2048; }
-__host__ __device__ constexpr int red_bytes(int NT) { return kWarps * NT * 8 * 64 * 4; }
+__host__ __device__ constexpr int red_bytes(int NT) { return warps_for(NT) * NT * 8 * 64 * 4; }
 
 struct Split {
     uint32_t hi, lo; // bf16 bits
@@ -86,19 +88,25 @@ __device__ __forceinline__ void store_split(uint8_t *dst, float4 xa, float4 xb)
     sts128(dst + 512, make_uint4(lw[0], lw[1], lw[2], lw[3]));
 }
 
-// Stage the CTA's K slice of X (pairs p0 .. p0+P-1): real tokens from global
-// memory (item = (q, blk, token, quad), kStageUnroll items' loads in flight
-// per thread), padded token lanes and padded K as zeros.
-template <int NT>
+// Stage the CTA's K slice of X (pairs p0 .. p0+P-1): the region is zeroed
+// (padded token lanes and padded K stay zero), then the real tokens are read
+// from global memory, item = (q, blk, token, quad), with kStageUnroll items'
+// loads in flight per thread.
+template <int NT, int THREADS>
 __device__ __forceinline__ void stage_x(const DecodeArgs &a, uint8_t *xs, int p0, int P)
 {
     const int m = a.m;
+    if (m < NT * 8) {
+        const int vecs = P * xs_pair_bytes(NT) / 16;
+        for (int i = threadIdx.x; i < vecs; i += THREADS) sts128(xs + i * 16, make_uint4(0u, 0u, 0u, 0u));
+        __syncthreads();
+    }
     const int real = P * 2 * m * 4;
-    for (int base = threadIdx.x; base < real; base += kThreads * kStageUnroll) {
+    for (int base = threadIdx.x; base < real; base += THREADS * kStageUnroll) {
         float4 xa[kStageUnroll], xb[kStageUnroll];
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
-            const int it = base + u * kThreads;
+            const int it = base + u * THREADS;
             xa[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             xb[u] = xa[u];
             if (it < real) {
@@ -116,25 +124,13 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, uint8_t *xs, int p0
         }
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
-            const int it = base + u * kThreads;
+            const int it = base + u * THREADS;
             if (it < real) {
                 const int c = it & 3;
                 const int tok = (it >> 2) % m;
                 const int qb = (it >> 2) / m;
                 store_split(xs_slot(xs, NT, qb >> 1, tok, qb & 1, c), xa[u], xb[u]);
             }
-        }
-    }
-    const int pad = NT * 8 - m;
-    if (pad > 0) {
-        const int items = P * 2 * pad * 4;
-        for (int it = threadIdx.x; it < items; it += kThreads) {
-            const int c = it & 3;
-            const int tok = m + (it >> 2) % pad;
-            const int qb = (it >> 2) / pad;
-            uint8_t *dst = xs_slot(xs, NT, qb >> 1, tok, qb & 1, c);
-            sts128(dst, make_uint4(0u, 0u, 0u, 0u));
-            sts128(dst + 512, make_uint4(0u, 0u, 0u, 0u));
         }
     }
 }
@@ -204,8 +200,10 @@ __device__ __forceinline__ float ld_cg(const float *p)
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(warps_for(NT) * 32, 1) decode_kernel(const DecodeArgs a)
 {
+    constexpr int kWarps = warps_for(NT);
+    constexpr int kThreads = kWarps * 32;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_last;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,9 +233,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     fence_barrier_init();
     __syncthreads();
 
-    // Everything below reads global memory the previous kernel may write.
-    pdl_wait();
-
     const uint64_t pol = policy_evict_first();
     int issued = 0;
     auto issue = [&](int j) {
@@ -249,10 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
         mbar_arrive_expect_tx(&mybar[slot], kPairBytes);
         bulk_g2s_hint(myring + slot * kPairBytes, src, kPairBytes, &mybar[slot], pol);
     };
+    // The weights may be streamed before the preceding kernel in the stream
+    // has finished only when the caller declared them read-only; X, Y and the
+    // workspace are touched after the wait.
+    if (a.prefetch_w && lane == 0)
+        for (; issued < min(STG, J); ++issued) issue(issued);
+    pdl_wait();
     if (lane == 0)
         for (; issued < min(STG, J); ++issued) issue(issued);
 
-    stage_x<NT>(a, xs, p0, P);
+    stage_x<NT, kThreads>(a, xs, p0, P);
     __syncthreads();
 
     const int m = a.m;
@@ -366,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 size_t decode_smem_bytes(int NT, int P, int stages)
 {
     const size_t xs = static_cast<size_t>(round_up(static_cast<int64_t>(P) * xs_pair_bytes(NT), 1024));
-    return 1024 /* alignment slack */ + xs + static_cast<size_t>(kWarps) * stages * kPairBytes + red_bytes(NT) +
-           static_cast<size_t>(kWarps) * stages * 8;
+    const size_t warps = static_cast<size_t>(warps_for(NT));
+    return 1024 /* alignment slack */ + xs + warps * stages * kPairBytes + red_bytes(NT) + warps * stages * 8;
 }
 
 // Choose the K split S and the grid. Cost model: the busiest SM's pair loads,
@@ -384,25 +385,30 @@ bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan
         if (S > 1 && groups > kDecodeCounterSlots) break;
         const int64_t P = ceil_div(np, S);
         if (S > 1 && ceil_div(np, S - 1) == P) continue; // same slice width, more slices
-        const int64_t WQ = ceil_div(P, kWarps);
-        int stages = 4;
+        const int64_t WQ = ceil_div(P, warps_for(NT));
+        if (decode_smem_bytes(NT, static_cast<int>(P), 1) > kSmemOptIn) continue;
+        // deepest ring that fits (at most every job of a warp, at most 8)
+        int stages = 1;
+        while (stages < 8 && decode_smem_bytes(NT, static_cast<int>(P), stages + 1) <= kSmemOptIn) ++stages;
         size_t smem = decode_smem_bytes(NT, static_cast<int>(P), stages);
-        if (smem > kSmemOptIn) continue;
-        int64_t r = std::min<int64_t>(8, static_cast<int64_t>(kSmemPerSM / (smem + 1024)));
+        int64_t r = std::min<int64_t>(2048 / (warps_for(NT) * 32), static_cast<int64_t>(kSmemPerSM / (smem + 1024)));
         int64_t cps = std::min<int64_t>(groups, std::max<int64_t>(1, sm_count * r / S));
         int64_t ng = ceil_div(groups, cps);
         const int64_t jobs = ng * WQ;
         if (jobs < stages) {
             stages = static_cast<int>(std::max<int64_t>(1, jobs));
             smem = decode_smem_bytes(NT, static_cast<int>(P), stages);
-            r = std::min<int64_t>(8, static_cast<int64_t>(kSmemPerSM / (smem + 1024)));
+            r = std::min<int64_t>(2048 / (warps_for(NT) * 32), static_cast<int64_t>(kSmemPerSM / (smem + 1024)));
             cps = std::min<int64_t>(groups, std::max<int64_t>(1, sm_count * r / S));
             ng = ceil_div(groups, cps);
         }
         const int64_t ctas = cps * S;
         const int64_t per_sm = ceil_div(ctas, sm_count);
         const double overhead = 1.0 + (S > 1 ? 2.0 : 0.0);
-        const double cost = static_cast<double>(per_sm) * ng * (static_cast<double>(P) + overhead);
+        // a ring shallower than three stages leaves the memory pipe idle
+        const int64_t want = std::min<int64_t>(3, ng * WQ);
+        const double shallow = 1.0 + 0.25 * static_cast<double>(std::max<int64_t>(0, want - stages));
+        const double cost = static_cast<double>(per_sm) * ng * (static_cast<double>(P) + overhead) * shallow;
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best.NT = NT;
@@ -435,7 +441,7 @@ cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaSt
     if (e != cudaSuccess) return e;
     DecodeArgs a = args;
     void *kargs[] = {&a};
-    return launch_pdl(fn, dim3(plan.ctas), dim3(kThreads), plan.smem, s, kargs);
+    return launch_pdl(fn, dim3(plan.ctas), dim3(warps_for(plan.NT) * 32), plan.smem, s, kargs);
 }
 
 } // namespace q4

@@ -64,6 +64,7 @@ struct DecodeArgs {
     int S, pbase, prem;    // K slices: slice s has pbase + (s < prem) pairs
     int stages;            // ring depth per warp
     int xs_bytes;          // shared bytes reserved for the staged X slice
+    int prefetch_w;        // stream W before waiting on the preceding kernel
 };
 
 struct DecodePlan {

@@ -13,9 +13,10 @@
 //   2. gemm: one CTA per (128 weight rows) x (T tokens). Warp roles:
 //        warp 0     producer: bulk copies of raw packed W records and X tiles
 //        warp 1     TMEM allocation and the single MMA-issuing thread
-//        warps 2-5  dequantise W (split-half nibbles -> bf16 (q-8)*d, rounded
-//                   once) into 128B-swizzled K-major shared tiles, then the
-//                   epilogue (TMEM -> registers -> Y)
+//        warps 2-9  dequantise W (split-half nibbles -> exact bf16 (q-8),
+//                   times d rounded to bf16) into 128B-swizzled K-major shared
+//                   tiles, one 16-row tile per warp, then the epilogue
+//                   (TMEM -> registers -> Y), two warps per TMEM sub-partition
 //      tcgen05.mma kind::f16 (bf16 x bf16, fp32 accumulate in TMEM), M = 128
 //      weight rows, N = T tokens (split into 256 + rest when T > 256).
 //      Every ring is an mbarrier pipeline; every wait is time-bounded.
@@ -29,7 +30,8 @@ namespace q4 {
 namespace {
 
 constexpr int kErrTimeout = 5;
-constexpr int kGemmThreads = 192;
+constexpr int kDequantWarps = 8;
+constexpr int kGemmThreads = (2 + kDequantWarps) * 32;
 constexpr int kAStageBytes = 128 * 128; // 128 rows x 64 bf16
 
 // ------------------------------------------------------------- xcast -----
@@ -84,21 +86,12 @@ __device__ __forceinline__ void fail(const Smem &sm, const PrefillArgs &a)
     record_status(a.status, kErrTimeout);
 }
 
-// bf16 (q-8) * d, rounded once: d = dhi + dlo exactly (dlo has <= 3 bits), so
-// v*dlo is exact and fma(v, dhi, v*dlo) rounds the exact product once.
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, uint32_t dhi2, uint32_t dlo2)
+// bf16 (q-8) times d: d is rounded to bf16 and the product rounded once,
+// so |w - (q-8)*d| <= 2^-8 |(q-8)*d|; (q-8) itself is exact.
+__device__ __forceinline__ uint32_t scale_splat_bf16(float d)
 {
-    return bf16x2_fma(v, dhi2, bf16x2_mul(v, dlo2));
-}
-
-__device__ __forceinline__ void split_scale(float d, uint32_t &dhi2, uint32_t &dlo2)
-{
-    const uint32_t hi = bf16_rn_bits(d);
-    const float dhi = __uint_as_float(hi << 16);
-    const float r = d - dhi; // exact; not finite only when d is not
-    const uint32_t lo = isfinite(r) ? bf16_rn_bits(r) : 0u;
-    dhi2 = hi | (hi << 16);
-    dlo2 = lo | (lo << 16);
+    const uint32_t h = bf16_rn_bits(d);
+    return h | (h << 16);
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const PrefillArgs a)
@@ -132,8 +125,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const PrefillArgs
 
     if (tid == 0) {
         for (int i = 0; i < a.rb; ++i) mbar_init(&sm.full_b[i], 1), mbar_init(&sm.empty_b[i], 1);
-        for (int i = 0; i < a.ra; ++i) mbar_init(&sm.full_a[i], 4), mbar_init(&sm.empty_a[i], 1);
-        for (int i = 0; i < a.rw; ++i) mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], 4);
+        for (int i = 0; i < a.ra; ++i) mbar_init(&sm.full_a[i], kDequantWarps), mbar_init(&sm.empty_a[i], 1);
+        for (int i = 0; i < a.rw; ++i) mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], kDequantWarps);
         mbar_init(sm.done, 1);
         *sm.abort = 0;
         fence_barrier_init();
@@ -147,32 +140,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const PrefillArgs
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_slot;
 
+    // The raw weight records never come from the preceding kernel (that is
+    // always this call's X cast, which writes only the X image), so the first
+    // weight stages are requested before the dependency wait.
+    const uint8_t *xsrc = a.ximg + static_cast<size_t>(jt) * np * bstage;
+    const uint32_t wbytes = (has_g1 ? 2u : 1u) * kPairBytes;
+    auto issue_w = [&](int p, uint64_t pol) {
+        const int sw = p % a.rw;
+        mbar_arrive_expect_tx(&sm.full_w[sw], wbytes);
+        uint8_t *wdst = sm.w + static_cast<size_t>(sw) * 2 * kPairBytes;
+        bulk_g2s_hint(wdst, a.W + (static_cast<int64_t>(G0) * np + p) * kPairBytes, kPairBytes, &sm.full_w[sw], pol);
+        if (has_g1)
+            bulk_g2s_hint(wdst + kPairBytes, a.W + (static_cast<int64_t>(G0 + 1) * np + p) * kPairBytes, kPairBytes,
+                          &sm.full_w[sw], pol);
+    };
+    int w_issued = 0;
+    if (warp == 0 && lane == 0) {
+        const uint64_t pol_w = policy_evict_last();
+        for (; w_issued < min(a.rw, np); ++w_issued) issue_w(w_issued, pol_w);
+    }
+
     pdl_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        int b_issued = 0, w_issued = 0;
+        int b_issued = 0;
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_last();
             const uint64_t pol_x = policy_evict_last();
-            const uint8_t *xsrc = a.ximg + static_cast<size_t>(jt) * np * bstage;
-            const uint32_t wbytes = (has_g1 ? 2u : 1u) * kPairBytes;
             for (int p = 0; p < np && !aborted(sm); ++p) {
-                const int sw = p % a.rw, sb = p % a.rb;
-                if (!mbar_wait(&sm.empty_w[sw], ((p / a.rw) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
-                mbar_arrive_expect_tx(&sm.full_w[sw], wbytes);
-                uint8_t *wdst = sm.w + static_cast<size_t>(sw) * 2 * kPairBytes;
-                bulk_g2s_hint(wdst, a.W + (static_cast<int64_t>(G0) * np + p) * kPairBytes, kPairBytes,
-                              &sm.full_w[sw], pol_w);
-                if (has_g1)
-                    bulk_g2s_hint(wdst + kPairBytes, a.W + (static_cast<int64_t>(G0 + 1) * np + p) * kPairBytes,
-                                  kPairBytes, &sm.full_w[sw], pol_w);
-                ++w_issued;
+                const int sb = p % a.rb;
                 if (!mbar_wait(&sm.empty_b[sb], ((p / a.rb) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
                 mbar_arrive_expect_tx(&sm.full_b[sb], bstage);
                 bulk_g2s_hint(sm.b + static_cast<size_t>(sb) * bstage, xsrc + static_cast<size_t>(p) * bstage, bstage,
                               &sm.full_b[sb], pol_x);
                 ++b_issued;
+                // refill the weight slot that stage p used once it is free
+                const int pw = p + a.rw;
+                if (pw < np) {
+                    if (!mbar_wait(&sm.empty_w[p % a.rw], (p / a.rw) & 1, a.wait_ns)) { fail(sm, a); break; }
+                    issue_w(pw, pol_w);
+                    ++w_issued;
+                }
             }
             // drain our copies before the CTA may exit
             for (int i = 0; i < a.rw; ++i) {
@@ -219,43 +228,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const PrefillArgs
         __syncwarp();
     } else {
         // ----------------------------------------------- dequantise W, epilogue
-        const int dw = warp - 2;
+        const int tt = warp - 2; // 16-row tile of this warp, 0..7
+        const int grp = tt >> 2;
         const int g = lane >> 2, c4 = lane & 3;
+        const bool have = grp == 0 || has_g1;
         for (int p = 0; p < np && !aborted(sm); ++p) {
             const int sw = p % a.rw, sa = p % a.ra;
             if (!mbar_wait(&sm.full_w[sw], (p / a.rw) & 1, a.wait_ns)) { fail(sm, a); break; }
             if (!mbar_wait(&sm.empty_a[sa], ((p / a.ra) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
             const uint8_t *wst = sm.w + static_cast<size_t>(sw) * 2 * kPairBytes;
             uint8_t *ast = sm.a + static_cast<size_t>(sa) * kAStageBytes;
+            uint4 nib = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+            uint2 sc = make_uint2(0u, 0u);
+            if (have) {
+                const uint8_t *rec = wst + grp * kPairBytes + (tt & 3) * kRecordBytes;
+                nib = lds128(rec + 64 + lane * 16);
+                sc = lds64(rec + g * 8);
+            }
+            // o[h][blk]: 8 weights of row (g + 8h), block blk, elements 4c4 + {0,2,16,18,1,3,17,19}
+            const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+            const uint32_t sbits[4] = {sc.x & 0xFFFF, sc.x >> 16, sc.y & 0xFFFF, sc.y >> 16};
+            uint4 o[2][2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int tt = 2 * dw + u; // tile of 16 rows, 0..7
-                const int grp = tt >> 2;
-                uint4 nib = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                uint2 sc = make_uint2(0u, 0u);
-                if (grp == 0 || has_g1) {
-                    const uint8_t *rec = wst + grp * kPairBytes + (tt & 3) * kRecordBytes;
-                    nib = lds128(rec + 64 + lane * 16);
-                    sc = lds64(rec + g * 8);
-                }
-                const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
-                const uint32_t sbits[4] = {sc.x & 0xFFFF, sc.x >> 16, sc.y & 0xFFFF, sc.y >> 16};
+            for (int i = 0; i < 4; ++i) {
+                const int blk = i >> 1, h = i & 1;
+                const uint32_t dd =
+                    scale_splat_bf16(__half2float(__ushort_as_half(static_cast<unsigned short>(sbits[i]))));
+                uint32_t v[4];
+                unpack_word_bf16(words[i], v);
+                o[h][blk] = make_uint4(bf16x2_mul(v[0], dd), bf16x2_mul(v[1], dd), bf16x2_mul(v[2], dd),
+                                       bf16x2_mul(v[3], dd));
+            }
+            // Store order: lanes of odd g write the other block first, so each
+            // 8-lane phase of a 16-byte store hits 8 distinct bank groups.
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int blk = i >> 1, h = i & 1;
-                    uint32_t dhi2, dlo2;
-                    split_scale(__half2float(__ushort_as_half(static_cast<unsigned short>(sbits[i]))), dhi2, dlo2);
-                    uint32_t v[4];
-                    unpack_word_bf16(words[i], v);
-                    uint4 o;
-                    o.x = scale_bf16x2(v[0], dhi2, dlo2);
-                    o.y = scale_bf16x2(v[1], dhi2, dlo2);
-                    o.z = scale_bf16x2(v[2], dhi2, dlo2);
-                    o.w = scale_bf16x2(v[3], dhi2, dlo2);
-                    const int row = tt * 16 + g + 8 * h;
-                    const int chunk = blk * 4 + c4;
-                    sts128(ast + row * 128 + ((chunk ^ (row & 7)) << 4), o);
-                }
+            for (int i = 0; i < 4; ++i) {
+                const int h = i & 1;
+                const int blk = (i >> 1) ^ (g & 1);
+                const int row = tt * 16 + g + 8 * h;
+                const int chunk = blk * 4 + c4;
+                sts128(ast + row * 128 + ((chunk ^ (row & 7)) << 4), blk ? o[h][1] : o[h][0]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -265,14 +277,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const PrefillArgs
             }
         }
 
-        // epilogue: rows of this warp's TMEM sub-partition
+        // epilogue: this warp's TMEM sub-partition, half of the token columns
         const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const int64_t grow = static_cast<int64_t>(rt) * 128 + row;
         if (!mbar_wait(sm.done, 0, a.wait_ns)) fail(sm, a);
         tc_fence_after();
         pdl_launch_dependents();
-        for (int c0 = 0; c0 < T; c0 += 16) {
+        const int chunks = T / 16;
+        const int c_lo = half * ((chunks + 1) / 2), c_hi = half ? chunks : (chunks + 1) / 2;
+        for (int cc = c_lo; cc < c_hi; ++cc) {
+            const int c0 = cc * 16;
             uint32_t r[16];
             tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c0), r);
             tmem_wait_ld();

@@ -218,6 +218,26 @@ def test_bitwise_deterministic(q4lib, m, n, k):
     assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (16, 1000, 2080)])
+def test_weight_prefetch_mode_gives_identical_results(q4lib, oracle_mod, m, n, k):
+    """Streaming W before the preceding kernel finishes changes timing only."""
+    blocks = synth.q4_0_blocks(n, k, seed=81)
+    X = synth.activations(m, k, seed=82)
+    W = pack_dev(q4lib, blocks, n, k)
+    torch.cuda.synchronize()
+    Y0 = run_matmul(q4lib, W, X, n)
+    try:
+        q4lib.q4_set_weight_prefetch(True)
+        Y1 = run_matmul(q4lib, W, X, n)
+        Y2 = run_matmul(q4lib, W, X, n)
+    finally:
+        q4lib.q4_set_weight_prefetch(False)
+    assert np.array_equal(Y0.view(np.uint32), Y1.view(np.uint32))
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y1, Yr, B, m, "prefetch mode")
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(q4lib, oracle_mod):
     import time
     q4lib.q4_last_device_status(clear=True)
