@@ -74,18 +74,16 @@ typedef struct CUstream_st *q4mm_stream_t;
  * kernel interface": a second, packed-weight interface). The payload is the
  * same 18 bytes per block; only padding is added.
  *
- *   n is padded to a multiple of 64 rows, k to a multiple of 64 (a pair of
- *   blocks). A record covers one tile of 16 rows x one pair of blocks and is
- *   576 bytes:
- *     bytes 0..63    32 fp16 scales; scale s = 4*g + 2*blk + h is d of row
- *                    (tile start + g + 8*h), block (2*pair + blk), g < 8.
- *     bytes 64..575  32 lanes x 16 bytes; lane L = 4*g + c holds the 4-byte
- *                    words qs[4c..4c+3] of (row g, blk 0), (row g+8, blk 0),
- *                    (row g, blk 1), (row g+8, blk 1), rows relative to the
- *                    tile start.
- *   Records are ordered [64-row group][pair][tile 0..3]: one group's data is
- *   contiguous and one pair of a group is 2304 contiguous bytes.
- *   Padding blocks have d = 0 and every nibble 8 (weight 0).
+ *   n is padded to a multiple of 128 rows (a group), k to a multiple of 64 (a
+ *   pair of blocks). A record covers one group x one pair and is 4608 bytes:
+ *     bytes    0..511   4 bytes per row r (at 4r): the fp16 scale bits of the
+ *                       pair's first block (low half) and second block
+ *                       (high half)
+ *     bytes  512..2559  16 bytes per row r (at 512 + 16r): qs of the first block
+ *     bytes 2560..4607  16 bytes per row r (at 2560 + 16r): qs of the second
+ *   Records are ordered [group][pair], so a group's pairs are contiguous and a
+ *   kernel thread that owns one row reads its share with three conflict-free
+ *   shared-memory loads. Padding blocks have d = 0 and every nibble 8.
  */
 
 /* Bytes of the packed form of an n x k Q4_0 matrix; 0 if n <= 0, k <= 0
@@ -108,7 +106,8 @@ Q4MM_API int q4_0_unpack(void *blocks, const void *W_packed, int64_t n, int64_t 
                          q4mm_stream_t stream);
 
 /* Bytes of device scratch q4_0_matmul_ws / q4_0_matmul_batched_slots_ws need
- * for these sizes (0 when the call needs none). */
+ * for these sizes: 0 for m <= 16 (decode needs none), the bf16 X image plus a
+ * 256 KB reserved region for m > 16. */
 Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
 
 /* Y[m x n] = X[m x k] . W^T, W given in packed form.
@@ -116,13 +115,16 @@ Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
  *   X: device fp32 [m x k] row-major, 16-byte aligned.
  *   Y: device fp32 [m x n] row-major, overwritten (no accumulate); 4-byte aligned.
  *   m >= 0 (m == 0 does nothing), n >= 1, k >= 32, k % 32 == 0.
- * Precision: for m <= 16 X is used at 16 significant bits (a two-term bf16
- * split of each fp32 value) with exact integer weights, the block scale
- * applied in fp32 and fp32 accumulation: |Y - Y_exact| <= 1e-3 * B + 1e-5
- * with B = sum_c |X[t][c] * W[j][c]|. For m > 16 X is rounded to bf16
- * (nearest even), each weight is the exact (q - 8) times d rounded to bf16,
- * rounded to bf16 (relative error <= 2^-8), and the tensor cores accumulate
- * in fp32: |Y - Y_exact| <= 1e-2 * B + 1e-4.
+ * Precision: for m <= 16 each weight is (q - 8) * d rounded once to fp16
+ * (relative error <= 2^-11), each X row is scaled by a power of two and split
+ * into two fp16 terms (22 significant bits relative to the row's largest
+ * |x|), and the tensor cores accumulate in fp32: |Y - Y_exact| <= 1e-3 * B +
+ * 1e-5 with B = sum_c |X[t][c] * W[j][c]|, for scales |d| <= 4096 (larger
+ * scales overflow fp16) and rows whose nonzero |x| do not span more than
+ * about 2^20. For m > 16 X is rounded to bf16 (nearest even), each weight is
+ * the exact (q - 8) times d rounded to bf16, rounded to bf16 (relative error
+ * <= 2^-8), and the tensor cores accumulate in fp32: |Y - Y_exact| <= 1e-2 *
+ * B + 1e-4. NaN and infinity in X propagate as in IEEE arithmetic.
  * Scratch: this form uses a workspace the library allocates on the current
  * device, once per (device, stream), grown when a call needs more. A call
  * that has to grow it synchronises `stream` and is refused with
@@ -189,6 +191,15 @@ Q4MM_API int q4_set_wait_limit_ns(uint64_t ns);
  * The prefill path always overlaps its weight reads: the kernel before its
  * GEMM is its own X cast. Applies to launches made after the call. */
 Q4MM_API int q4_set_weight_prefetch(int enable);
+
+/* Profiling builds only (compiled with -DQ4MM_TRACE): kernels launched after
+ * the call write 16-byte event records {globaltimer ns, event << 16 | warp
+ * << 8 | lane, argument} for the CTA with blockIdx.x == cta into `buffer`
+ * (device memory, 16-byte aligned, zeroed by the caller), split into 64
+ * equal regions, one per recording thread (lanes 0..3 of warps 0..15); a
+ * zero timestamp ends a region. NULL switches tracing off. Normal builds
+ * return Q4_ERR_INVALID_ARG. */
+Q4MM_API int q4_debug_set_trace(void *buffer, size_t bytes, uint32_t cta);
 
 /* Self-test of the bounded-wait path: launches one block that waits on a
  * barrier nothing ever completes, for at most limit_ns nanoseconds, then

@@ -243,59 +243,47 @@ int q4o_dequant_matrix(const uint8_t *blocks, int64_t n, int64_t k, double *W)
  * "The pluggable kernel interface": packing weights at load) but leave the
  * layout to the implementation. Specification:
  *
- *   rows are padded to a multiple of 64, k to a multiple of 64;
- *   a record covers 16 rows (a tile) x 2 blocks (a pair) and is 576 bytes:
- *     bytes 0..63:   32 scales, index s = g*4 + blk*2 + h holds the fp16 bits
- *                    of d(row = tile0 + g + 8h, block = 2p + blk)
- *     bytes 64..575: 32 lanes x 16 bytes, lane L = 4g + c holds the 4-byte
- *                    words qs[4c..4c+3] of (row g, blk 0), (row g+8, blk 0),
- *                    (row g, blk 1), (row g+8, blk 1) in that order;
- *   records are ordered [row group of 64 rows][pair][tile 0..3];
+ *   rows are padded to a multiple of 128, k to a multiple of 64;
+ *   a record covers 128 rows (a group) x 2 blocks (a pair) and is 4608 bytes:
+ *     bytes    0..511   per row r: 4 bytes, the fp16 scale bits of block 2p
+ *                       (low half) and of block 2p+1 (high half)
+ *     bytes  512..2559  per row r: qs[16] of block 2p
+ *     bytes 2560..4607  per row r: qs[16] of block 2p+1
+ *   records are ordered [group][pair];
  *   padding blocks have d = 0 and every nibble 8.
  */
 size_t q4o_packed_size(int64_t n, int64_t k)
 {
     if (n <= 0 || k <= 0 || (k % 32) != 0) return 0;
-    const int64_t groups = (n + 63) / 64, pairs = (k + 63) / 64;
-    return (size_t)(groups * pairs * 4 * 576);
+    const int64_t groups = (n + 127) / 128, pairs = (k + 63) / 64;
+    return (size_t)(groups * pairs * 4608);
 }
 
 int q4o_pack_reference(const uint8_t *blocks, int64_t n, int64_t k, uint8_t *packed)
 {
     if (n <= 0 || k <= 0 || (k % 32) != 0) return -1;
     const int64_t nb = k / 32;
-    const int64_t groups = (n + 63) / 64, pairs = (k + 63) / 64;
+    const int64_t groups = (n + 127) / 128, pairs = (k + 63) / 64;
     for (int64_t G = 0; G < groups; ++G)
-        for (int64_t p = 0; p < pairs; ++p)
-            for (int t = 0; t < 4; ++t) {
-                uint8_t *rec = packed + ((G * pairs + p) * 4 + t) * 576;
-                for (int g = 0; g < 8; ++g)
-                    for (int blk = 0; blk < 2; ++blk)
-                        for (int h = 0; h < 2; ++h) {
-                            const int64_t row = G * 64 + t * 16 + g + 8 * h;
-                            const int64_t b = 2 * p + blk;
-                            const int s = g * 4 + blk * 2 + h;
-                            uint8_t lo = 0, hi = 0;
-                            if (row < n && b < nb) {
-                                const uint8_t *src = blocks + (row * nb + b) * 18;
-                                lo = src[0], hi = src[1];
-                            }
-                            rec[2 * s] = lo, rec[2 * s + 1] = hi;
-                        }
-                for (int L = 0; L < 32; ++L) {
-                    const int g = L / 4, c = L % 4;
-                    for (int w = 0; w < 4; ++w) {
-                        const int blk = w / 2, h = w % 2;
-                        const int64_t row = G * 64 + t * 16 + g + 8 * h;
-                        const int64_t b = 2 * p + blk;
-                        uint8_t *dst = rec + 64 + L * 16 + w * 4;
-                        if (row < n && b < nb)
-                            memcpy(dst, blocks + (row * nb + b) * 18 + 2 + 4 * c, 4);
-                        else
-                            memset(dst, 0x88, 4);
+        for (int64_t p = 0; p < pairs; ++p) {
+            uint8_t *rec = packed + (G * pairs + p) * 4608;
+            for (int r = 0; r < 128; ++r) {
+                const int64_t row = G * 128 + r;
+                for (int blk = 0; blk < 2; ++blk) {
+                    const int64_t b = 2 * p + blk;
+                    uint8_t *sc = rec + 4 * r + 2 * blk;
+                    uint8_t *qs = rec + 512 + 2048 * blk + 16 * r;
+                    if (row < n && b < nb) {
+                        const uint8_t *src = blocks + (row * nb + b) * 18;
+                        sc[0] = src[0], sc[1] = src[1];
+                        memcpy(qs, src + 2, 16);
+                    } else {
+                        sc[0] = 0, sc[1] = 0;
+                        memset(qs, 0x88, 16);
                     }
                 }
             }
+        }
     return 0;
 }
 

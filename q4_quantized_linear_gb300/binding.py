@@ -16,8 +16,10 @@ import ctypes
 import os
 import threading
 
-from .build import LIB
+from .build import LIB as _DEFAULT_LIB
 
+# Q4MM_LIBRARY selects another build of the same ABI (e.g. a profiling build).
+LIB = os.environ.get("Q4MM_LIBRARY", _DEFAULT_LIB)
 if not os.path.exists(LIB):
     raise ImportError(
         f"libq4mm is not built ({LIB} missing); run `python -m q4_quantized_linear_gb300.build`")
@@ -43,6 +45,7 @@ _SIGS = {
     "q4_set_wait_limit_ns": (_INT, [ctypes.c_uint64]),
     "q4_set_weight_prefetch": (_INT, [_INT]),
     "q4_selftest_wait_timeout": (_INT, [ctypes.c_uint64, _P]),
+    "q4_debug_set_trace": (_INT, [_P, _SZ, ctypes.c_uint32]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -159,6 +162,11 @@ def q4_set_wait_limit_ns(ns: int) -> int:
 
 def q4_set_weight_prefetch(enable: bool) -> int:
     return _check(_lib.q4_set_weight_prefetch(1 if enable else 0), "q4_set_weight_prefetch")
+
+
+def q4_debug_set_trace(buffer, nbytes: int, cta: int = 0, check: bool = True) -> int:
+    rc = _lib.q4_debug_set_trace(_addr(buffer), nbytes, cta)
+    return _check(rc, "q4_debug_set_trace") if check else rc
 
 
 def q4_selftest_wait_timeout(limit_ns: int, stream=None) -> int:

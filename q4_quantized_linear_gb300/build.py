@@ -17,6 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libq4mm.so")
+TRACE_BUILD = os.path.join(PKG, "_build_trace")
+TRACE_LIB = os.path.join(TRACE_BUILD, "libq4mm.so")
 HEADER = os.path.join(ROOT, "include", "q4mm.h")
 
 SOURCES = ["q4mm_api.cu", "q4mm_pack.cu", "q4mm_decode.cu", "q4mm_prefill.cu"]
@@ -41,12 +43,12 @@ def _stale(target: str, inputs: list[str]) -> bool:
     return any(os.path.getmtime(i) > t for i in inputs)
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose_ptxas: bool, outdir: str = BUILD, extra: tuple = ()) -> str:
+    obj = os.path.join(outdir, os.path.splitext(src)[0] + ".o")
     inputs = [os.path.join(CSRC, src), HEADER] + [os.path.join(CSRC, d) for d in DEPS] + [__file__]
     if not _stale(obj, inputs):
         return obj
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose_ptxas else []) + \
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + (["-Xptxas", "-v"] if verbose_ptxas else []) + \
         ["-c", os.path.join(CSRC, src), "-o", obj + ".tmp"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -57,27 +59,31 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False) -> str:
+    """Compile libq4mm. trace=True makes the profiling build (in-kernel event
+    trace, -DQ4MM_TRACE) in a separate directory."""
+    outdir, lib = (TRACE_BUILD, TRACE_LIB) if trace else (BUILD, LIB)
+    extra = ("-DQ4MM_TRACE",) if trace else ()
+    os.makedirs(outdir, exist_ok=True)
     if force:
-        for f in os.listdir(BUILD):
+        for f in os.listdir(outdir):
             if f.endswith(".o"):
-                os.remove(os.path.join(BUILD, f))
+                os.remove(os.path.join(outdir, f))
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    if force or _stale(LIB, objs):
-        vscript = os.path.join(BUILD, "exports.map")
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, outdir, extra), SOURCES))
+    if force or _stale(lib, objs):
+        vscript = os.path.join(outdir, "exports.map")
         with open(vscript, "w") as f:
             f.write("{ global: q4_*; local: *; };\n")
-        tmp = LIB + f".tmp{os.getpid()}"
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + \
             ["-Xlinker", f"--version-script={vscript}"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -26,6 +26,8 @@ constexpr int64_t kDecodeMaxM = 16;
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 std::atomic<int> g_prefetch_w{0};
+std::mutex g_trace_mutex;
+TraceSettings g_trace;
 
 struct DeviceSlot {
     std::once_flag once;
@@ -136,10 +138,7 @@ int library_workspace(int dev, cudaStream_t s, size_t need, void **out)
 size_t workspace_size(int64_t m, int64_t k, int64_t n, int sm_count)
 {
     if (m <= 0) return 0;
-    if (m <= kDecodeMaxM) {
-        DecodePlan p;
-        return plan_decode(m, k, n, sm_count, &p) ? p.ws_bytes : 0;
-    }
+    if (m <= kDecodeMaxM) return 0;
     PrefillPlan p;
     return plan_prefill(m, k, n, sm_count, &p) ? p.ws_bytes : 0;
 }
@@ -159,14 +158,9 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     const uint64_t wait_ns = g_wait_ns.load();
 
     if (m <= kDecodeMaxM) {
+        // the decode path needs no scratch: K slices meet in cluster shared memory
         DecodePlan plan;
         if (!plan_decode(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
-        if (library_ws) {
-            rc = library_workspace(dev.device, s, plan.ws_bytes, &workspace);
-            if (rc != Q4_OK) return rc;
-            ws_bytes = plan.ws_bytes;
-        }
-        if (plan.ws_bytes > 0 && (!workspace || ws_bytes < plan.ws_bytes)) return Q4_ERR_WORKSPACE;
         DecodeArgs a{};
         a.W = static_cast<const uint8_t *>(W);
         a.X = X;
@@ -174,11 +168,6 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.ldx = ldx;
         a.Y = Y;
         a.ldy = ldy;
-        a.partials = plan.ws_bytes ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + plan.ws_partials_off)
-                                   : nullptr;
-        a.counters = plan.ws_bytes
-                         ? reinterpret_cast<unsigned *>(static_cast<uint8_t *>(workspace) + plan.ws_counters_off)
-                         : nullptr;
         a.status = dev.status;
         a.wait_ns = wait_ns;
         a.m = static_cast<int>(m);
@@ -186,11 +175,6 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.nb = static_cast<int>(k / 32);
         a.np = static_cast<int>(ceil_div(k, kPairK));
         a.groups = static_cast<int>(ceil_div(n, kGroupRows));
-        a.S = plan.S;
-        a.pbase = plan.pbase;
-        a.prem = plan.prem;
-        a.stages = plan.stages;
-        a.xs_bytes = plan.xs_bytes;
         a.prefetch_w = g_prefetch_w.load();
         return map_cuda(launch_decode(plan, a, s));
     }
@@ -227,14 +211,18 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     pa.groups = static_cast<int>(ceil_div(n, kGroupRows));
     pa.T = plan.T;
     pa.ts = plan.ts;
-    pa.rb = plan.rb;
-    pa.ra = plan.ra;
-    pa.rw = plan.rw;
-    pa.tmem_cols = plan.tmem_cols;
+    pa.ring = plan.ring;
+    pa.astages = plan.astages;
     return map_cuda(launch_prefill(plan, xa, pa, s));
 }
 
 } // namespace
+
+TraceSettings trace_settings()
+{
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    return g_trace;
+}
 
 cudaError_t set_max_smem(const void *func, size_t bytes)
 {
@@ -261,18 +249,28 @@ cudaError_t set_max_smem(const void *func, size_t bytes)
     return bytes <= it->second ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void **args)
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void **args,
+                       int cluster_x)
 {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_x > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelExC(&cfg, func, args);
 }
 
@@ -285,7 +283,7 @@ extern "C" {
 Q4MM_API size_t q4_0_packed_size(int64_t n, int64_t k)
 {
     if (!valid_nk(n, k)) return 0;
-    return static_cast<size_t>(ceil_div(n, kGroupRows) * ceil_div(k, kPairK) * kPairBytes);
+    return static_cast<size_t>(ceil_div(n, kGroupRows) * ceil_div(k, kPairK) * kRecordBytes);
 }
 
 Q4MM_API int q4_0_pack(void *W_packed, const void *blocks, int64_t n, int64_t k, q4mm_stream_t stream)
@@ -402,6 +400,25 @@ Q4MM_API int q4_set_weight_prefetch(int enable)
 {
     g_prefetch_w.store(enable ? 1 : 0);
     return Q4_OK;
+}
+
+Q4MM_API int q4_debug_set_trace(void *buffer, size_t bytes, uint32_t cta)
+{
+#ifdef Q4MM_TRACE
+    std::lock_guard<std::mutex> lock(g_trace_mutex);
+    if (!buffer || bytes < 64) {
+        g_trace = TraceSettings{};
+        return Q4_OK;
+    }
+    if (!aligned(buffer, 16)) return Q4_ERR_ALIGNMENT;
+    g_trace.buf = static_cast<unsigned long long *>(buffer);
+    g_trace.cap = static_cast<unsigned>(bytes / 16 / 64); // 64 regions
+    g_trace.cta = cta;
+    return Q4_OK;
+#else
+    (void)buffer, (void)bytes, (void)cta;
+    return Q4_ERR_INVALID_ARG;
+#endif
 }
 
 Q4MM_API int q4_selftest_wait_timeout(uint64_t limit_ns, q4mm_stream_t stream)

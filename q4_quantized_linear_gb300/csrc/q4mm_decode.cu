@@ -6,28 +6,29 @@
 // cost what one did on the card) and goinfer ch. 10 ("What the kernels are")
 // calls the quantised GEMV the decode workhorse.
 //
-// Design (GB300, one kernel per call):
-//   * Persistent CTAs of 16 warps (8 when m > 8). CTA c owns a K
-//     slice (when one is needed) and a strided set of 64-row groups. Each
-//     warp streams its own share of every group's pairs (2304 contiguous
-//     bytes per pair) through a private ring of shared-memory stages filled
-//     by 1-D bulk async copies (TMA engine, L2 evict-first), so each SM keeps
-//     tens of KB of weight reads in flight.
-//   * X is staged once per CTA for its K slice: each fp32 value becomes a
-//     two-term bf16 split (hi = truncation, lo = rounded remainder, 16
-//     significant bits) laid out in mma fragment order. All of a thread's
-//     global loads are issued before any is used, so staging costs about one
-//     memory latency, and it overlaps the first weight copies.
-//   * The split-half nibbles become exact bf16 (q - 8) in registers (mask
-//     into a biased exponent, subtract 136); warp-level bf16 MMAs
-//     (m16n8k16, fp32 accumulate) form each block's exact integer-weighted
-//     partial sum, which is scaled by the block's fp16 d in fp32 and
-//     accumulated. Tensor cores here only replace CUDA-core FMAs: the kernel
-//     stays bound by the weight bytes.
-//   * The warps' partials of a group are added in a fixed order through
-//     shared memory. With K slices, each slice writes its partial to the
-//     workspace and the last slice to finish (a counter) adds all slices in
-//     slice order, so results are bitwise reproducible.
+// Design (GB300, one kernel per call and K range):
+//   * A CTA owns 128 weight rows (one packed group) and a slice of K; the
+//     slices of a group form one thread-block cluster (up to 8 CTAs).
+//   * Warp 0: four producer lanes, each owning every fourth pair, stream the
+//     4608-byte packed records through a shared-memory ring with 1-D bulk
+//     copies (several independent rings keep tens of KB in flight per SM).
+//   * Warps 2-9: each thread owns one weight row; it turns the pair's 64
+//     split-half nibbles into fp16 (q - 8) * d, rounded once, and stores them
+//     straight into tensor memory (tcgen05.st). No warp waits on a tensor
+//     core result, so the CUDA cores only stream.
+//   * Warp 1: one thread issues tcgen05.mma kind::f16: A = those weights
+//     from tensor memory, B = X from shared memory, D = 128 x N fp32 in
+//     tensor memory.
+//   * Warps 10-13 stage X once per CTA while the first weights stream and
+//     dequantise: every token row is scaled by a power of two (its largest
+//     |x| in the slice lands in [2^14, 2^15)) and split into fp16 hi + lo,
+//     22 significant bits, as the N = 16 (m <= 8) or N = 32 rows of the B
+//     operand. They then run the epilogue.
+//   * Epilogue: y = (D_hi + D_lo) / scale. Slices of a cluster add their
+//     partial rows into the first CTA's shared memory (DSMEM) and that CTA
+//     sums them in slice order, so results are bitwise reproducible and no
+//     global scratch is needed. K ranges too long for one cluster run as
+//     further launches that add into Y in order.
 #include <algorithm>
 #include <cuda_runtime.h>
 
@@ -38,410 +39,459 @@ namespace q4 {
 namespace {
 
 constexpr int kErrTimeout = 5; // Q4_ERR_DEVICE_TIMEOUT
-constexpr int kStageUnroll = 4; // X items whose loads are in flight together
+constexpr int kDequantWarps = 8;
+constexpr int kXWarps = 4;          // stage X, then the epilogue (one per TMEM sub-partition)
+constexpr int kXWarp0 = 2 + kDequantWarps;
+constexpr int kXThreads = kXWarps * 32;
+constexpr int kThreads = (2 + kDequantWarps + kXWarps) * 32;
+constexpr int kProducerLanes = 4;
+constexpr int kAStages = 7;        // weight stages in tensor memory (32 columns each)
+constexpr int kAcol0 = 32;         // D uses columns 0..31
+constexpr uint32_t kTmemCols = 256;
+constexpr int kStageUnroll = 4;
+constexpr int kMaxSlices = 8;
 
-// Warps per CTA: 16 (four per SM sub-partition, at most 128 registers) for
-// one n-tile; 8 for two n-tiles, whose accumulators need more registers.
-__host__ __device__ constexpr int warps_for(int NT) { return NT == 1 ? 16 : 8; }
+// X image: per pair, N rows (hi tokens, then lo tokens) x 128 bytes, 128-byte
+// swizzle, chunk c = 4 blk + quad holding block elements 4 quad + {0,2,16,18,
+// 1,3,17,19}: the order dequant_pair_f16 writes the weights in.
+__device__ __forceinline__ uint32_t ximg_off(int N, int q, int row, int c)
+{
+    return static_cast<uint32_t>(q * N * 128 + row * 128 + ((c ^ (row & 7)) << 4));
+}
 
-// Shared-memory bytes of the X region per pair: NT x 2 blocks x (hi, lo) x 512.
-__host__ __device__ constexpr int xs_pair_bytes(int NT) { return NT * 2048; }
-__host__ __device__ constexpr int red_bytes(int NT) { return warps_for(NT) * NT * 8 * 64 * 4; }
+__device__ __forceinline__ uint32_t f16_bits(float x)
+{
+    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
+}
 
-struct Split {
-    uint32_t hi, lo; // bf16 bits
+// hi + lo fp16 split of an already scaled value.
+__device__ __forceinline__ void split_f16(float xs, uint32_t &hi, uint32_t &lo)
+{
+    hi = f16_bits(xs);
+    const float r = xs - __half2float(__ushort_as_half(static_cast<unsigned short>(hi)));
+    lo = isfinite(r) ? f16_bits(r) : 0u;
+}
+
+// One row's pair of blocks -> 32 fp16x2 columns of tensor memory (same
+// column order as the X image): (q - 8) exact, times d, rounded once.
+__device__ __forceinline__ void dequant_pair_f16(uint32_t d01, uint4 q0, uint4 q1, uint32_t out[32])
+{
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const uint32_t h = blk ? (d01 >> 16) : (d01 & 0xFFFFu);
+        const uint32_t dd = h | (h << 16);
+        const uint4 q = blk ? q1 : q0;
+        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+            uint32_t v[4];
+            unpack_word_f16(words[wd], v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) out[blk * 16 + wd * 4 + j] = hmul2_bits(v[j], dd);
+        }
+    }
+}
+
+struct Smem {
+    uint8_t *xs, *w;
+    float *red;
+    uint64_t *full_w, *empty_w, *full_a, *empty_a, *done, *x_ready;
+    uint32_t *tmem_slot;
+    int *abort;
+    unsigned *maxbits;    // [16] largest |x| bits per token
+    float *scale_up;      // [16] 2^e per token
+    float *scale_dn;      // [16] 2^-e per token
 };
 
-// x = hi + lo with hi the bf16 truncation of x and lo the remainder rounded to
-// bf16: 16 significant bits in all, and no overflow near FLT_MAX.
-__device__ __forceinline__ Split split_bf16(float x)
+__device__ __forceinline__ bool aborted(const Smem &sm) { return *reinterpret_cast<volatile int *>(sm.abort) != 0; }
+
+__device__ __forceinline__ void fail(const Smem &sm, const DecodeArgs &a)
 {
-    uint32_t u = __float_as_uint(x);
-    uint32_t hb = u & 0xFFFF0000u;
-    float r = x - __uint_as_float(hb);
-    if (!isfinite(x)) {
-        r = 0.0f;
-        if (isnan(x)) hb = 0x7FC00000u;
-    }
-    return {hb >> 16, bf16_rn_bits(r)};
+    *reinterpret_cast<volatile int *>(sm.abort) = 1;
+    record_status(a.status, kErrTimeout);
 }
 
-// Fragment-order X region: [pair q][n-tile][blk][hi | lo][lane][16 B]; lane
-// L = 4g + c holds token (8 nt + g), block elements 4c + {0,2,16,18,1,3,17,19}.
-__device__ __forceinline__ uint8_t *xs_slot(uint8_t *xs, int NT, int q, int tok, int blk, int c)
+__device__ __forceinline__ void xwarps_sync()
 {
-    const int nt = tok >> 3, L = ((tok & 7) << 2) | c;
-    return xs + ((q * NT + nt) * 2 + blk) * 1024 + L * 16;
+    asm volatile("bar.sync 2, %0;" ::"n"(kXThreads) : "memory");
 }
 
-__device__ __forceinline__ void store_split(uint8_t *dst, float4 xa, float4 xb)
+// Stage the slice of X (pairs p0 .. p0+P-1) as the scaled fp16 hi/lo image.
+// Run by the kXThreads threads of the X warps; xt is the thread's index among
+// them.
+template <int N>
+__device__ __forceinline__ void stage_x(const DecodeArgs &a, const Smem &sm, int p0, int P, int xt)
 {
-    const float v[8] = {xa.x, xa.z, xb.x, xb.z, xa.y, xa.w, xb.y, xb.w};
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const Split s0 = split_bf16(v[2 * i]), s1 = split_bf16(v[2 * i + 1]);
-        hw[i] = s0.hi | (s1.hi << 16);
-        lw[i] = s0.lo | (s1.lo << 16);
-    }
-    sts128(dst, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-    sts128(dst + 512, make_uint4(lw[0], lw[1], lw[2], lw[3]));
-}
-
-// Stage the CTA's K slice of X (pairs p0 .. p0+P-1): the region is zeroed
-// (padded token lanes and padded K stay zero), then the real tokens are read
-// from global memory, item = (q, blk, token, quad), with kStageUnroll items'
-// loads in flight per thread.
-template <int NT, int THREADS>
-__device__ __forceinline__ void stage_x(const DecodeArgs &a, uint8_t *xs, int p0, int P)
-{
+    constexpr int MP = N / 2;
     const int m = a.m;
-    if (m < NT * 8) {
-        const int vecs = P * xs_pair_bytes(NT) / 16;
-        for (int i = threadIdx.x; i < vecs; i += THREADS) sts128(xs + i * 16, make_uint4(0u, 0u, 0u, 0u));
-        __syncthreads();
+    const int lane = xt & 31;
+    const int kslice = P * 64;
+    const int64_t col0 = static_cast<int64_t>(p0) * 64;
+    const int64_t kreal = static_cast<int64_t>(a.nb) * 32;
+    // 1. largest |x| of each token over the slice
+    for (int t = 0; t < m; ++t) {
+        const int64_t row = a.rows ? static_cast<int64_t>(a.rows[t]) : t;
+        const float *xr = a.X + row * a.ldx + col0;
+        unsigned mx = 0;
+        for (int i = xt; i < kslice / 4; i += kXThreads) {
+            if (col0 + 4 * i < kreal) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(xr) + i);
+                mx = max(mx, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+                                 max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (lane == 0) atomicMax(&sm.maxbits[t], mx);
     }
-    const int real = P * 2 * m * 4;
-    for (int base = threadIdx.x; base < real; base += THREADS * kStageUnroll) {
+    // zero the image (padded token rows and padded K stay zero)
+    if (m < MP) {
+        const int vecs = P * N * 8;
+        for (int i = xt; i < vecs; i += kXThreads) sts128(sm.xs + i * 16, make_uint4(0u, 0u, 0u, 0u));
+    }
+    xwarps_sync();
+    // 2. per-token power of two: largest |x| into [2^14, 2^15)
+    if (xt < m) {
+        const unsigned mb = sm.maxbits[xt];
+        int e = 0;
+        if (mb != 0 && mb < 0x7F800000u) {
+            const int E = static_cast<int>(mb >> 23) - 126; // |x|max = f * 2^E, f in [0.5, 1) (normal)
+            e = (mb >> 23) == 0 ? 100 : 15 - E;
+            e = max(-100, min(100, e));
+        }
+        sm.scale_up[xt] = __uint_as_float(static_cast<unsigned>(e + 127) << 23);
+        sm.scale_dn[xt] = __uint_as_float(static_cast<unsigned>(127 - e) << 23);
+    }
+    xwarps_sync();
+    // 3. the split, item = (pair q, token t, chunk c); loads of kStageUnroll
+    //    items in flight per thread
+    const int items = P * m * 8;
+    for (int base = xt; base < items; base += kXThreads * kStageUnroll) {
         float4 xa[kStageUnroll], xb[kStageUnroll];
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
-            const int it = base + u * THREADS;
+            const int it = base + u * kXThreads;
             xa[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             xb[u] = xa[u];
-            if (it < real) {
-                const int c = it & 3;
-                const int tok = (it >> 2) % m;
-                const int qb = (it >> 2) / m; // q * 2 + blk
-                const int b = 2 * p0 + qb;
+            if (it < items) {
+                const int c = it & 7, t = (it >> 3) % m, q = (it >> 3) / m;
+                const int b = 2 * (p0 + q) + (c >> 2);
                 if (b < a.nb) {
-                    const int64_t row = a.rows ? static_cast<int64_t>(a.rows[tok]) : tok;
-                    const float *xr = a.X + row * a.ldx + 32 * b;
-                    xa[u] = __ldg(reinterpret_cast<const float4 *>(xr + 4 * c));
-                    xb[u] = __ldg(reinterpret_cast<const float4 *>(xr + 16 + 4 * c));
+                    const int64_t row = a.rows ? static_cast<int64_t>(a.rows[t]) : t;
+                    const float *xr = a.X + row * a.ldx + 32 * b + 4 * (c & 3);
+                    xa[u] = __ldg(reinterpret_cast<const float4 *>(xr));
+                    xb[u] = __ldg(reinterpret_cast<const float4 *>(xr + 16));
                 }
             }
         }
 #pragma unroll
         for (int u = 0; u < kStageUnroll; ++u) {
-            const int it = base + u * THREADS;
-            if (it < real) {
-                const int c = it & 3;
-                const int tok = (it >> 2) % m;
-                const int qb = (it >> 2) / m;
-                store_split(xs_slot(xs, NT, qb >> 1, tok, qb & 1, c), xa[u], xb[u]);
+            const int it = base + u * kXThreads;
+            if (it < items) {
+                const int c = it & 7, t = (it >> 3) % m, q = (it >> 3) / m;
+                const float su = sm.scale_up[t];
+                const float v[8] = {xa[u].x, xa[u].z, xb[u].x, xb[u].z, xa[u].y, xa[u].w, xb[u].y, xb[u].w};
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t h0, l0, h1, l1;
+                    split_f16(v[2 * i] * su, h0, l0);
+                    split_f16(v[2 * i + 1] * su, h1, l1);
+                    hw[i] = h0 | (h1 << 16);
+                    lw[i] = l0 | (l1 << 16);
+                }
+                sts128(sm.xs + ximg_off(N, q, t, c), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                sts128(sm.xs + ximg_off(N, q, MP + t, c), make_uint4(lw[0], lw[1], lw[2], lw[3]));
             }
         }
     }
+    // generic-proxy writes -> visible to the tensor core's shared-memory reads
+    fence_proxy_async_smem();
+    xwarps_sync();
+    if (xt == 0) mbar_arrive(sm.x_ready);
 }
 
-__device__ __forceinline__ float half_lo(uint32_t w)
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
 {
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFF)));
-}
-__device__ __forceinline__ float half_hi(uint32_t w)
-{
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
-}
-
-// One pair (2 blocks) of one 64-row group for this warp: 4 tiles of 16 rows.
-template <int NT>
-__device__ __forceinline__ void compute_pair(const uint8_t *st, const uint8_t *xq, int lane, float (&acc)[4][NT][4])
-{
-    const int g = lane >> 2;
-    uint4 xh[2][NT], xl[2][NT];
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint8_t *p = xq + (nt * 2 + blk) * 1024 + lane * 16;
-            xh[blk][nt] = lds128(p);
-            xl[blk][nt] = lds128(p + 512);
-        }
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const uint8_t *rec = st + t * kRecordBytes;
-        const uint4 nib = lds128(rec + 64 + lane * 16);
-        const uint2 sc = lds64(rec + g * 8);
-        const float ds[2][2] = {{half_lo(sc.x), half_hi(sc.x)}, {half_lo(sc.y), half_hi(sc.y)}};
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            uint32_t va[4], vb[4];
-            unpack_word_bf16(blk ? nib.z : nib.x, va); // row g
-            unpack_word_bf16(blk ? nib.w : nib.y, vb); // row g + 8
-            const uint32_t A0[4] = {va[0], vb[0], va[1], vb[1]};
-            const uint32_t A1[4] = {va[2], vb[2], va[3], vb[3]};
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_bf16_16816(c, A0, xh[blk][nt].x, xh[blk][nt].y, c);
-                mma_bf16_16816(c, A0, xl[blk][nt].x, xl[blk][nt].y, c);
-                mma_bf16_16816(c, A1, xh[blk][nt].z, xh[blk][nt].w, c);
-                mma_bf16_16816(c, A1, xl[blk][nt].z, xl[blk][nt].w, c);
-                acc[t][nt][0] = fmaf(ds[blk][0], c[0], acc[t][nt][0]);
-                acc[t][nt][1] = fmaf(ds[blk][0], c[1], acc[t][nt][1]);
-                acc[t][nt][2] = fmaf(ds[blk][1], c[2], acc[t][nt][2]);
-                acc[t][nt][3] = fmaf(ds[blk][1], c[3], acc[t][nt][3]);
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-__device__ __forceinline__ float ld_cg(const float *p)
-{
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    return v;
-}
-
-template <int NT>
-__global__ void __launch_bounds__(warps_for(NT) * 32, 1) decode_kernel(const DecodeArgs a)
-{
-    constexpr int kWarps = warps_for(NT);
-    constexpr int kThreads = kWarps * 32;
+    constexpr int MP = N / 2;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int s_last;
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.S;
-    const int s = blockIdx.x % S;
-    const int cps = gridDim.x / S;
-    const int cidx = blockIdx.x / S;
-    const int p0 = s * a.pbase + min(s, a.prem);
-    const int P = a.pbase + (s < a.prem ? 1 : 0);
-    const int wq0 = warp * (P / kWarps) + min(warp, P % kWarps);
-    const int WQ = P / kWarps + (warp < P % kWarps ? 1 : 0);
-    const int ng = cidx < a.groups ? (a.groups - cidx + cps - 1) / cps : 0;
-    const int J = ng * WQ;
-    const int STG = a.stages;
-
-    uint8_t *xs = smem;
-    uint8_t *ring = smem + a.xs_bytes;
-    float *red = reinterpret_cast<float *>(ring + kWarps * STG * kPairBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(red) + red_bytes(NT));
-    uint64_t *mybar = bars + warp * STG;
-    uint8_t *myring = ring + warp * STG * kPairBytes;
-
-    if (lane == 0)
-        for (int i = 0; i < STG; ++i) mbar_init(&mybar[i], 1);
-    fence_barrier_init();
-    __syncthreads();
-
-    const uint64_t pol = policy_evict_first();
-    int issued = 0;
-    auto issue = [&](int j) {
-        const int gi = j / WQ, q = j % WQ;
-        const int64_t G = cidx + static_cast<int64_t>(gi) * cps;
-        const int pp = p0 + wq0 + q;
-        const uint8_t *src = a.W + (G * a.np + pp) * kPairBytes;
-        const int slot = j % STG;
-        mbar_arrive_expect_tx(&mybar[slot], kPairBytes);
-        bulk_g2s_hint(myring + slot * kPairBytes, src, kPairBytes, &mybar[slot], pol);
-    };
-    // The weights may be streamed before the preceding kernel in the stream
-    // has finished only when the caller declared them read-only; X, Y and the
-    // workspace are touched after the wait.
-    if (a.prefetch_w && lane == 0)
-        for (; issued < min(STG, J); ++issued) issue(issued);
-    pdl_wait();
-    if (lane == 0)
-        for (; issued < min(STG, J); ++issued) issue(issued);
-
-    stage_x<NT, kThreads>(a, xs, p0, P);
-    __syncthreads();
-
+    const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int G = blockIdx.x / S;                   // 128-row group
+    const int p0 = a.pass_p0 + rank * a.pbase + min(rank, a.prem);
+    const int P = a.pbase + (rank < a.prem ? 1 : 0);
+    const int R = a.ring;
     const int m = a.m;
-    const int n_pad = a.groups * 64;
-    const int per = NT * 8 * 64;
-    bool ok = true;
-    int j = 0;
-    for (int gi = 0; gi < ng; ++gi) {
-        float acc[4][NT][4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[t][nt][i] = 0.f;
+    const TraceRef tr{a.trace_buf, a.trace_cap, a.trace_cta};
+    trace_init();
+    if (tid == 0) trace(tr, kTrStart, 0);
 
-        for (int q = 0; q < WQ; ++q, ++j) {
-            const int slot = j % STG;
-            if (ok && !mbar_wait(&mybar[slot], static_cast<uint32_t>((j / STG) & 1), a.wait_ns)) {
-                ok = false;
-                record_status(a.status, kErrTimeout);
+    Smem sm;
+    sm.xs = base;
+    sm.w = sm.xs + a.xs_bytes;
+    sm.red = reinterpret_cast<float *>(sm.w + static_cast<size_t>(R) * kRecordBytes);
+    const int red_floats = S > 1 ? (S - 1) * m * 128 : 0;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.red + red_floats + (red_floats & 1));
+    sm.full_w = bars;
+    sm.empty_w = sm.full_w + R;
+    sm.full_a = sm.empty_w + R;
+    sm.empty_a = sm.full_a + kAStages;
+    sm.done = sm.empty_a + kAStages;
+    sm.x_ready = sm.done + 1;
+    sm.tmem_slot = reinterpret_cast<uint32_t *>(sm.x_ready + 1);
+    sm.abort = reinterpret_cast<int *>(sm.tmem_slot + 1);
+    sm.maxbits = reinterpret_cast<unsigned *>(sm.abort + 1);
+    sm.scale_up = reinterpret_cast<float *>(sm.maxbits + 16);
+    sm.scale_dn = sm.scale_up + 16;
+
+    if (tid == 0) {
+        for (int i = 0; i < R; ++i) mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], kDequantWarps / 2);
+        for (int i = 0; i < kAStages; ++i) mbar_init(&sm.full_a[i], kDequantWarps / 2), mbar_init(&sm.empty_a[i], 1);
+        mbar_init(sm.done, 1);
+        mbar_init(sm.x_ready, 1);
+        *sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (tid < 16) sm.maxbits[tid] = 0u;
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (S > 1) cluster_sync(); // every CTA of the cluster is running before any DSMEM traffic
+    const uint32_t tmem = *sm.tmem_slot;
+
+    const uint8_t *wsrc = a.W + (static_cast<int64_t>(G) * a.np + p0) * kRecordBytes;
+    const bool producer = warp == 0 && lane < kProducerLanes;
+    const uint64_t pol = policy_evict_first();
+    int w_next = lane; // producer lane: next pair (relative to p0) to issue
+    auto issue = [&](int j) {
+        const int s = j % R;
+        trace(tr, kTrWIssue, static_cast<unsigned>(j));
+        mbar_arrive_expect_tx(&sm.full_w[s], kRecordBytes);
+        bulk_g2s_hint(sm.w + static_cast<size_t>(s) * kRecordBytes, wsrc + static_cast<size_t>(j) * kRecordBytes,
+                      kRecordBytes, &sm.full_w[s], pol);
+    };
+
+    // Weights may stream before the preceding kernel has finished only when
+    // the caller declared them read-only; X and Y are touched after the wait.
+    if (producer && a.prefetch_w)
+        for (; w_next < P && w_next < R; w_next += kProducerLanes) issue(w_next);
+    pdl_wait();
+    if (tid == 0) trace(tr, kTrPdl, 0);
+    if (producer)
+        for (; w_next < P && w_next < R; w_next += kProducerLanes) issue(w_next);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (producer) {
+            int last = w_next - kProducerLanes;
+            for (int j = w_next; j < P && !aborted(sm); j += kProducerLanes) {
+                if (!mbar_wait(&sm.empty_w[j % R], ((j / R) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
+                issue(j);
+                last = j;
             }
-            compute_pair<NT>(myring + slot * kPairBytes, xs + (wq0 + q) * xs_pair_bytes(NT), lane, acc);
+            for (int j = last; j >= 0 && j > last - R; j -= kProducerLanes)
+                if (!mbar_wait(&sm.full_w[j % R], (j / R) & 1, a.wait_ns)) fail(sm, a);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // --------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(128, N);
+            const uint32_t xs0 = smem_u32(sm.xs);
+            if (P > 0 && !mbar_wait(sm.x_ready, 0, a.wait_ns)) fail(sm, a);
+            for (int j = 0; j < P && !aborted(sm); ++j) {
+                const int sa = j % kAStages;
+                if (!mbar_wait(&sm.full_a[sa], (j / kAStages) & 1, a.wait_ns)) { fail(sm, a); break; }
+                trace(tr, kTrMmaIssue, static_cast<unsigned>(j));
+                tc_fence_after();
+                const uint32_t at = tmem + kAcol0 + static_cast<uint32_t>(sa) * 32u;
+                const uint32_t bs = xs0 + static_cast<uint32_t>(j * N * 128);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16_ts(tmem, at + 8 * kk, smem_desc_sw128(bs + kk * 32), idesc, (j | kk) != 0);
+                tc_commit(&sm.empty_a[sa]);
+            }
+            tc_commit(sm.done); // also taken on abort: no MMA of ours is in flight past this
+        }
+        __syncwarp();
+    } else if (warp >= kXWarp0) {
+        // ------------------------------------------------------------ stage X
+        stage_x<N>(a, sm, p0, P, tid - kXWarp0 * 32);
+        if (tid == kXWarp0 * 32) trace(tr, kTrXStaged, 0);
+    } else {
+        // -------------------------------------------------------- dequantise
+        const int dw = warp - 2;
+        const int q = warp & 3;
+        const int h = dw >> 2;
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        for (int j = h; j < P && !aborted(sm); j += 2) {
+            const int sw = j % R, sa = j % kAStages;
+            if (!mbar_wait(&sm.full_w[sw], (j / R) & 1, a.wait_ns)) { fail(sm, a); break; }
+            if (lane == 0) trace(tr, kTrWFull, static_cast<unsigned>(j));
+            if (!mbar_wait(&sm.empty_a[sa], ((j / kAStages) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
+            const uint8_t *rec = sm.w + static_cast<size_t>(sw) * kRecordBytes;
+            const uint32_t d01 = *reinterpret_cast<const uint32_t *>(rec + kRecScaleOff + 4 * row);
+            const uint4 q0 = lds128(rec + kRecQs0Off + 16 * row);
+            const uint4 q1 = lds128(rec + kRecQs1Off + 16 * row);
+            uint32_t out[32];
+            dequant_pair_f16(d01, q0, q1, out);
+            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + static_cast<uint32_t>(sa) * 32u, out);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0 && ok && issued < J) issue(issued++);
-        }
-
-        // Fixed-order reduction of the 8 warps' partials of this group.
-        {
-            const int g = lane >> 2, c4 = lane & 3;
-            float *mine = red + warp * per;
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int tok = nt * 8 + 2 * c4;
-                    const int r0 = t * 16 + g;
-                    mine[tok * 64 + r0] = acc[t][nt][0];
-                    mine[(tok + 1) * 64 + r0] = acc[t][nt][1];
-                    mine[tok * 64 + r0 + 8] = acc[t][nt][2];
-                    mine[(tok + 1) * 64 + r0 + 8] = acc[t][nt][3];
-                }
-        }
-        named_barrier_sync(1, kThreads);
-
-        const int64_t G = cidx + static_cast<int64_t>(gi) * cps;
-        for (int e = tid; e < m * 64; e += kThreads) {
-            const int tok = e >> 6, row = e & 63;
-            float v = red[e];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) v += red[w * per + e];
-            const int64_t grow = G * 64 + row;
-            if (S == 1) {
-                if (grow < a.n) {
-                    const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[tok]) : tok;
-                    a.Y[yrow * a.ldy + grow] = v;
-                }
-            } else {
-                a.partials[(static_cast<int64_t>(s) * m + tok) * n_pad + grow] = v;
+            if (lane == 0) {
+                mbar_arrive(&sm.full_a[sa]);
+                mbar_arrive(&sm.empty_w[sw]);
+                trace(tr, kTrDeqDone, static_cast<unsigned>(j));
             }
         }
-        if (S > 1) {
-            __threadfence();
-            named_barrier_sync(1, kThreads);
-            if (tid == 0) {
-                const unsigned old = atomicAdd(&a.counters[G], 1u);
-                s_last = old == static_cast<unsigned>(S - 1);
-            }
-            named_barrier_sync(1, kThreads);
-            if (s_last) {
-                __threadfence();
-                for (int e = tid; e < m * 64; e += kThreads) {
-                    const int tok = e >> 6, row = e & 63;
-                    const int64_t grow = G * 64 + row;
-                    if (grow < a.n) {
-                        float v = 0.f;
-                        for (int ss = 0; ss < S; ++ss)
-                            v += ld_cg(a.partials + (static_cast<int64_t>(ss) * m + tok) * n_pad + grow);
-                        const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[tok]) : tok;
-                        a.Y[yrow * a.ldy + grow] = v;
-                    }
-                }
-                // every slice of this group has arrived: leave its counter at
-                // zero for the next call
-                if (tid == 0) a.counters[G] = 0u;
-            }
-        }
-        // the partials of this group must be read before the next is written
-        named_barrier_sync(1, kThreads);
     }
 
+    // ------------------------------------------------------------ epilogue
+    // the X warps cover the four TMEM sub-partitions: thread = weight row
+    const bool epi = warp >= kXWarp0;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int64_t grow = static_cast<int64_t>(G) * kGroupRows + row;
+    float y[MP];
+#pragma unroll
+    for (int t = 0; t < MP; ++t) y[t] = 0.f;
+    if (epi) {
+        if (!mbar_wait(sm.done, 0, a.wait_ns)) fail(sm, a);
+        if (lane == 0) trace(tr, kTrDone, 0);
+        tc_fence_after();
+        uint32_t d[N];
+        if constexpr (N == 16) {
+            tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(q * 32) << 16), d);
+        } else {
+            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16), d);
+        }
+        tmem_wait_ld();
+        if (P > 0) {
+#pragma unroll
+            for (int t = 0; t < MP; ++t)
+                if (t < m) y[t] = (__uint_as_float(d[t]) + __uint_as_float(d[MP + t])) * sm.scale_dn[t];
+        }
+        if (S > 1 && rank > 0) {
+            const uint32_t dst = mapa_shared(smem_u32(sm.red), 0u);
+#pragma unroll
+            for (int t = 0; t < MP; ++t)
+                if (t < m) st_cluster_f32(dst + static_cast<uint32_t>((((rank - 1) * m + t) * 128 + row) * 4), y[t]);
+        }
+    }
     pdl_launch_dependents();
-
-    // Drain: no bulk copy of ours may still be landing when the CTA exits.
-    if (lane == 0) {
-        for (int slot = 0; slot < STG; ++slot) {
-            int last = -1;
-            for (int jj = issued - 1; jj >= 0 && jj >= issued - STG; --jj)
-                if (jj % STG == slot) {
-                    last = jj;
-                    break;
-                }
-            if (last >= 0 && !mbar_wait(&mybar[slot], static_cast<uint32_t>((last / STG) & 1), a.wait_ns))
-                record_status(a.status, kErrTimeout);
+    if (S > 1) cluster_sync(); // partial rows have landed in the first CTA
+    if (epi && rank == 0 && grow < a.n) {
+#pragma unroll
+        for (int t = 0; t < MP; ++t) {
+            if (t < m) {
+                float v = y[t];
+                for (int rr = 1; rr < S; ++rr) v += sm.red[((rr - 1) * m + t) * 128 + row];
+                const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[t]) : t;
+                float *dst = a.Y + yrow * a.ldy + grow;
+                *dst = a.accumulate ? *dst + v : v;
+            }
         }
     }
+
+    if (epi && lane == 0) trace(tr, kTrEpiDone, 0);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0) trace(tr, kTrEnd, 0);
+}
+
+size_t decode_smem(int N, int P, int ring, int S, int64_t m)
+{
+    const size_t xs = static_cast<size_t>(round_up(static_cast<int64_t>(P) * N * 128, 1024));
+    const size_t red = S > 1 ? static_cast<size_t>(S - 1) * m * 128 * 4 + 8 : 0;
+    const size_t bars = static_cast<size_t>(2 * ring + 2 * kAStages + 2) * 8 + 16 + 48 * 4;
+    return 1024 + xs + static_cast<size_t>(ring) * kRecordBytes + red + bars;
 }
 
 } // namespace
 
-size_t decode_smem_bytes(int NT, int P, int stages)
-{
-    const size_t xs = static_cast<size_t>(round_up(static_cast<int64_t>(P) * xs_pair_bytes(NT), 1024));
-    const size_t warps = static_cast<size_t>(warps_for(NT));
-    return 1024 /* alignment slack */ + xs + warps * stages * kPairBytes + red_bytes(NT) + warps * stages * 8;
-}
-
-// Choose the K split S and the grid. Cost model: the busiest SM's pair loads,
-// plus a per-group overhead for the reduction (larger when slices must be
-// combined through the workspace).
+// Choose the cluster size S (K slices per 128-row group, at most 8) and the
+// number of launches over K: the busiest SM's pair count plus a per-CTA
+// start-up cost, with at most two CTAs per SM (tensor memory: 256 columns each).
 bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan)
 {
+    if (m < 1 || m > 16) return false;
+    const int N = m <= 8 ? 16 : 32;
+    const int64_t tiles = ceil_div(n, kGroupRows);
+    const int64_t np = ceil_div(k, kPairK);
+    const int64_t xs_budget = 96 * 1024;
+    const int64_t pmax = xs_budget / (N * 128);
     DecodePlan best;
     double best_cost = 1e300;
-    const int NT = m <= 8 ? 1 : 2;
-    const int64_t np = ceil_div(k, kPairK);
-    const int64_t groups = ceil_div(n, kGroupRows);
-    for (int64_t S = 1; S <= np && S <= 64; ++S) {
-        if (S > 1 && groups > kDecodeCounterSlots) break;
-        const int64_t P = ceil_div(np, S);
-        if (S > 1 && ceil_div(np, S - 1) == P) continue; // same slice width, more slices
-        const int64_t WQ = ceil_div(P, warps_for(NT));
-        if (decode_smem_bytes(NT, static_cast<int>(P), 1) > kSmemOptIn) continue;
-        // deepest ring that fits (at most every job of a warp, at most 8)
-        int stages = 1;
-        while (stages < 8 && decode_smem_bytes(NT, static_cast<int>(P), stages + 1) <= kSmemOptIn) ++stages;
-        size_t smem = decode_smem_bytes(NT, static_cast<int>(P), stages);
-        int64_t r = std::min<int64_t>(2048 / (warps_for(NT) * 32), static_cast<int64_t>(kSmemPerSM / (smem + 1024)));
-        int64_t cps = std::min<int64_t>(groups, std::max<int64_t>(1, sm_count * r / S));
-        int64_t ng = ceil_div(groups, cps);
-        const int64_t jobs = ng * WQ;
-        if (jobs < stages) {
-            stages = static_cast<int>(std::max<int64_t>(1, jobs));
-            smem = decode_smem_bytes(NT, static_cast<int>(P), stages);
-            r = std::min<int64_t>(2048 / (warps_for(NT) * 32), static_cast<int64_t>(kSmemPerSM / (smem + 1024)));
-            cps = std::min<int64_t>(groups, std::max<int64_t>(1, sm_count * r / S));
-            ng = ceil_div(groups, cps);
-        }
-        const int64_t ctas = cps * S;
-        const int64_t per_sm = ceil_div(ctas, sm_count);
-        const double overhead = 1.0 + (S > 1 ? 2.0 : 0.0);
-        // a ring shallower than three stages leaves the memory pipe idle
-        const int64_t want = std::min<int64_t>(3, ng * WQ);
-        const double shallow = 1.0 + 0.25 * static_cast<double>(std::max<int64_t>(0, want - stages));
-        const double cost = static_cast<double>(per_sm) * ng * (static_cast<double>(P) + overhead) * shallow;
+    for (int S = 1; S <= kMaxSlices; ++S) {
+        if (S > np) break;
+        const int64_t passes = ceil_div(np, S * pmax);
+        const int64_t ppp = ceil_div(np, passes);          // pairs per pass
+        if (ppp < S) continue;
+        const int64_t P = ceil_div(ppp, S);
+        const int ring = 8;
+        size_t smem = decode_smem(N, static_cast<int>(P), ring, S, m);
+        // at most two resident CTAs per SM, so that tensor memory always suffices
+        smem = std::max<size_t>(smem, kSmemPerSM / 3 + 1024);
+        if (smem > kSmemOptIn) continue;
+        const int64_t units = tiles * S;
+        const int64_t per_sm = ceil_div(units, sm_count);
+        const double cost = static_cast<double>(passes) * per_sm * (static_cast<double>(P) + 6.0 + (S > 1 ? 2.0 : 0.0));
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
-            best.NT = NT;
-            best.S = static_cast<int>(S);
-            best.pbase = static_cast<int>(np / S);
-            best.prem = static_cast<int>(np % S);
-            best.stages = stages;
-            best.ctas = static_cast<int>(ctas);
-            best.xs_bytes = static_cast<int>(round_up(P * xs_pair_bytes(NT), 1024));
+            best.N = N;
+            best.S = S;
+            best.passes = static_cast<int>(passes);
+            best.pairs_per_pass = static_cast<int>(ppp);
+            best.ring = ring;
+            best.ctas = static_cast<int>(units);
+            best.xs_bytes = static_cast<int>(round_up(P * N * 128, 1024));
             best.smem = smem;
         }
     }
     if (best.ctas == 0) return false;
-    if (best.S > 1) {
-        // counters first, at a fixed place, so they stay zero between calls of
-        // any shape; partials after them
-        best.ws_counters_off = 0;
-        best.ws_partials_off = kWsCounterBytes;
-        best.ws_bytes = best.ws_partials_off + static_cast<size_t>(best.S) * m * groups * 64 * sizeof(float);
-    }
     *plan = best;
     return true;
 }
 
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaStream_t s)
 {
-    const void *fn = plan.NT == 1 ? reinterpret_cast<const void *>(&decode_kernel<1>)
-                                  : reinterpret_cast<const void *>(&decode_kernel<2>);
+    const void *fn = plan.N == 16 ? reinterpret_cast<const void *>(&decode_kernel<16>)
+                                  : reinterpret_cast<const void *>(&decode_kernel<32>);
     cudaError_t e = set_max_smem(fn, plan.smem);
     if (e != cudaSuccess) return e;
-    DecodeArgs a = args;
-    void *kargs[] = {&a};
-    return launch_pdl(fn, dim3(plan.ctas), dim3(warps_for(plan.NT) * 32), plan.smem, s, kargs);
+    for (int pass = 0; pass < plan.passes; ++pass) {
+        DecodeArgs a = args;
+        a.pass_p0 = pass * plan.pairs_per_pass;
+        const int pp = std::min(plan.pairs_per_pass, args.np - a.pass_p0);
+        a.S = plan.S;
+        a.pbase = pp / plan.S;
+        a.prem = pp % plan.S;
+        a.accumulate = pass > 0 ? 1 : 0;
+        a.ring = plan.ring;
+        a.xs_bytes = plan.xs_bytes;
+        const TraceSettings ts = trace_settings();
+        a.trace_buf = ts.buf;
+        a.trace_cap = ts.cap;
+        a.trace_cta = ts.cta;
+        void *kargs[] = {&a};
+        e = launch_pdl(fn, dim3(plan.ctas), dim3(kThreads), plan.smem, s, kargs, plan.S);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 } // namespace q4

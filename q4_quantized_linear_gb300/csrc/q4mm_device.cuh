@@ -24,6 +24,59 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// In-kernel event trace (profiling builds only, -DQ4MM_TRACE). Records are
+// 16 bytes {globaltimer ns, event << 16 | warp << 8 | lane, argument}; each
+// recording thread (lanes 0..3 of a warp) owns a region of `cap` records in
+// the device buffer the host registered with q4_debug_set_trace, indexed by a
+// shared-memory counter, so recording is a fire-and-forget store. Only the
+// CTA chosen there records. Compiles to nothing in normal builds.
+struct TraceRef {
+    unsigned long long *buf; // regions of `cap` records, region = 4 * warp + lane
+    unsigned cap;            // records per region
+    unsigned cta;            // blockIdx.x that records
+};
+
+enum TraceEvent : unsigned {
+    kTrStart = 1, kTrPdl = 2, kTrXStaged = 3, kTrWIssue = 4, kTrWFull = 5, kTrDeqDone = 6,
+    kTrMmaIssue = 7, kTrBIssue = 8, kTrDone = 9, kTrEpiDone = 10, kTrEnd = 11, kTrBFull = 12
+};
+
+#ifdef Q4MM_TRACE
+__device__ __forceinline__ unsigned *trace_counters()
+{
+    __shared__ unsigned counters[64];
+    return counters;
+}
+#endif
+
+// Zero the per-region counters; call before the kernel's first barrier.
+__device__ __forceinline__ void trace_init()
+{
+#ifdef Q4MM_TRACE
+    if (threadIdx.x < 64) trace_counters()[threadIdx.x] = 0u;
+#endif
+}
+
+__device__ __forceinline__ void trace(const TraceRef &t, unsigned ev, unsigned arg)
+{
+#ifdef Q4MM_TRACE
+    const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (t.buf && blockIdx.x == t.cta && lane < 4 && warp < 16) {
+        const unsigned region = warp * 4 + lane;
+        const unsigned i = trace_counters()[region]++;
+        if (i < t.cap) {
+            unsigned long long now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            unsigned long long *r = t.buf + 2ull * (static_cast<unsigned long long>(region) * t.cap + i);
+            r[0] = now;
+            r[1] = (static_cast<unsigned long long>((ev << 16) | (warp << 8) | lane) << 32) | arg;
+        }
+    }
+#else
+    (void)t, (void)ev, (void)arg;
+#endif
+}
+
 // Record a device-side failure in the status word (first writer wins).
 __device__ __forceinline__ void record_status(int *status, int code)
 {
@@ -217,6 +270,46 @@ __device__ __forceinline__ void unpack_word_bf16(uint32_t w, uint32_t v[4])
     v[3] = bf16x2_sub(nib2_bf16_biased(w >> 12), k136);
 }
 
+// Same eight weights as fp16 (q - 8), exact. The high nibble of each byte is
+// taken in place at bits 4..7 of an fp16 mantissa (1024 + 16q) and brought
+// down by an exact fused multiply-add.
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t hfma2_bits(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t w, uint32_t mask, uint32_t magic)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(magic));
+    return r;
+}
+__device__ __forceinline__ void unpack_word_f16(uint32_t w, uint32_t v[4])
+{
+    const uint32_t magic = 0x64006400u;   // fp16 (1024, 1024)
+    const uint32_t k1032 = 0x64086408u;   // fp16 (1032, 1032)
+    const uint32_t k1_16 = 0x2C002C00u;   // fp16 (1/16, 1/16)
+    const uint32_t km72 = 0xD480D480u;    // fp16 (-72, -72)
+    const uint32_t w8 = w >> 8;
+    v[0] = hsub2_bits(lop3_and_or(w, 0x000F000Fu, magic), k1032);
+    v[1] = hfma2_bits(lop3_and_or(w, 0x00F000F0u, magic), k1_16, km72);
+    v[2] = hsub2_bits(lop3_and_or(w8, 0x000F000Fu, magic), k1032);
+    v[3] = hfma2_bits(lop3_and_or(w8, 0x00F000F0u, magic), k1_16, km72);
+}
+
 // --------------------------------------------------- warp-level bf16 MMA --
 
 // D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, fp32 accumulate.
@@ -285,6 +378,75 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t r[16
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 32 bits, 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t r[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Thread i of the warp writes its 32 registers to lane (base lane + i),
+// columns col..col+31.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t r[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (A read from tensor memory:
+// lane = row of A, column c = elements 2c, 2c+1 of that row's K).
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// ------------------------------------------------------------- clusters --
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA in the cluster arrives, then waits for all.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
 // swizzled canonical layout: rows of 128 bytes, 8-row atoms 1024 bytes apart.
 // The tile base must be 1024-byte aligned; K steps inside the 128-byte row
@@ -308,6 +470,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
            | (1u << 10)           // B format: bf16
            | ((N >> 3) << 17)     // N / 8
            | ((M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N)
+{
+    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 } // namespace q4

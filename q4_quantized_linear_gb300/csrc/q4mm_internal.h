@@ -9,21 +9,23 @@
 
 namespace q4 {
 
-constexpr int kRecordBytes = 576;     // one 16-row tile x one pair of blocks
-constexpr int kPairBytes = 4 * 576;   // one 64-row group x one pair of blocks
-constexpr int kGroupRows = 64;
+// Packed layout: records of 128 rows (a group) x 2 blocks (a pair).
+constexpr int kGroupRows = 128;
 constexpr int kPairK = 64;
+constexpr int kRecordBytes = 4608;     // 128 x 2 x 18
+constexpr int kRecScaleOff = 0;        // 4 bytes per row: fp16 d of block 0 | block 1
+constexpr int kRecQs0Off = 512;        // 16 bytes per row: qs of block 0
+constexpr int kRecQs1Off = 2560;       // 16 bytes per row: qs of block 1
+
 // 227 KB per CTA on sm_100-family parts, less room for a kernel's static
 // shared variables; plans never ask for more dynamic shared memory than this.
 constexpr size_t kSmemOptIn = 232448 - 256;
-constexpr size_t kSmemPerSM = 233472; // 228 KB per SM
-// Split-K counters of the decode kernel live in the first kDecodeCounterSlots
-// words of every workspace (one per 64-row group), so plans with K slices are
-// limited to n <= 64 * kDecodeCounterSlots rows. Every plan that uses a
-// workspace keeps this region in place (and only the decode kernel writes it,
-// leaving it zero), so calls of any shape can share one workspace.
-constexpr int64_t kDecodeCounterSlots = 65536;
-constexpr size_t kWsCounterBytes = kDecodeCounterSlots * 4;
+constexpr size_t kSmemPerSM = 233472;  // 228 KB per SM
+
+// Workspaces begin with a reserved, zeroed region (kept for split-sum
+// counters of any kernel that needs them), so calls of any shape can share
+// one buffer.
+constexpr size_t kWsReservedBytes = 256 * 1024;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -39,8 +41,17 @@ struct DeviceInfo {
 // (device, kernel).
 cudaError_t set_max_smem(const void *func, size_t bytes);
 
-// Launch helper: PDL-enabled launch on `stream`.
-cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void **args);
+// Event-trace destination the kernels record into (profiling builds only).
+struct TraceSettings {
+    unsigned long long *buf = nullptr;
+    unsigned cap = 0, cta = 0;
+};
+TraceSettings trace_settings();
+
+// Launch helper: programmatic-dependent launch on `stream`, optionally as
+// clusters of `cluster_x` CTAs along x.
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, void **args,
+                       int cluster_x = 1);
 
 // ------------------------------------------------------------------ pack --
 
@@ -56,32 +67,32 @@ struct DecodeArgs {
     int64_t ldx;
     float *Y;
     int64_t ldy;
-    float *partials;       // [S][m][groups*64] when S > 1
-    unsigned *counters;    // [groups] when S > 1
     int *status;
     uint64_t wait_ns;
     int m, n, nb, np, groups;
-    int S, pbase, prem;    // K slices: slice s has pbase + (s < prem) pairs
-    int stages;            // ring depth per warp
-    int xs_bytes;          // shared bytes reserved for the staged X slice
+    int pass_p0;           // first pair of this launch's K range
+    int S, pbase, prem;    // K slices of the range: slice s has pbase + (s < prem) pairs
+    int accumulate;        // add into Y instead of overwriting it
+    int ring;              // weight-record ring depth
+    int xs_bytes;          // shared bytes of the staged X image
     int prefetch_w;        // stream W before waiting on the preceding kernel
+    unsigned long long *trace_buf;
+    unsigned trace_cap, trace_cta;
 };
 
 struct DecodePlan {
-    int NT = 1;            // n8 token tiles (1: m <= 8, 2: m <= 16)
-    int S = 1;
-    int pbase = 0, prem = 0;
-    int stages = 8;
-    int ctas = 0;          // grid size (multiple of S)
+    int N = 16;            // MMA N: hi and lo rows of X, 16 (m <= 8) or 32
+    int S = 1;             // K slices = cluster size
+    int passes = 1;        // launches over consecutive K ranges
+    int pairs_per_pass = 0;
+    int ring = 8;
+    int ctas = 0;          // grid size per pass (tiles x S)
     int xs_bytes = 0;
     size_t smem = 0;
-    size_t ws_bytes = 0;   // workspace: partials + counters
-    size_t ws_partials_off = 0, ws_counters_off = 0;
 };
 
 bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan);
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaStream_t s);
-size_t decode_smem_bytes(int NT, int P, int stages);
 
 // --------------------------------------------------------------- prefill --
 
@@ -95,8 +106,10 @@ struct PrefillArgs {
     uint64_t wait_ns;
     int m, n, np, groups;
     int T, ts;              // tokens per tile, token tiles
-    int rb, ra, rw;         // ring depths: X tiles, dequantised W tiles, raw W records
-    int tmem_cols;
+    int ring;               // X-tile and weight-record ring depth
+    int astages;            // dequantised weight stages in tensor memory
+    unsigned long long *trace_buf;
+    unsigned trace_cap, trace_cta;
 };
 
 struct XcastArgs {
@@ -110,10 +123,9 @@ struct XcastArgs {
 struct PrefillPlan {
     int T = 0, ts = 0;
     int rowtiles = 0;
-    int rb = 0, ra = 0, rw = 0;
-    int tmem_cols = 0;
+    int ring = 0, astages = 0;
     size_t smem = 0;
-    size_t ws_bytes = 0;    // counter region + X image bytes
+    size_t ws_bytes = 0;    // reserved region + X image bytes
     size_t ws_ximg_off = 0;
 };
 

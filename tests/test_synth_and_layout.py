@@ -35,49 +35,44 @@ def test_slot_ids_distinct():
 
 
 def _locate(row, blk, elem):
-    """Byte offset and nibble shift of weight (row, blk, elem) in the packed
-    layout, from its specification (64-row groups, 64-k pairs, 16-row tiles,
-    576-byte records: 64 bytes of scales then 32 lanes x 16 bytes)."""
-    G, r = divmod(row, 64)
-    t, r16 = divmod(r, 16)
-    h, g = divmod(r16, 8)
+    """Record, byte offset and nibble shift of weight (row, blk, elem) in the
+    packed layout, from its specification (128-row groups, 64-k pairs,
+    4608-byte records: 512 bytes of scale pairs, then 16 bytes per row for the
+    pair's first block, then 16 bytes per row for its second)."""
+    G, r = divmod(row, 128)
     p, b2 = divmod(blk, 2)
-    byte_in_qs = elem % 16
     shift = 0 if elem < 16 else 4
-    c, byte_in_word = divmod(byte_in_qs, 4)
-    lane = 4 * g + c
-    word = b2 * 2 + h
-    return ((G, p, t), 64 + lane * 16 + word * 4 + byte_in_word, shift)
+    return (G, p), 512 + 2048 * b2 + 16 * r + elem % 16, shift
 
 
 def test_pack_reference_matches_specification(oracle_mod):
-    n, k = 70, 96            # ragged rows (70 = 64 + 6) and an odd block count (3)
+    n, k = 140, 96           # ragged rows (140 = 128 + 12) and an odd block count (3)
     blocks = synth.q4_0_blocks(n, k, seed=5)
     packed = oracle_mod.pack_reference(blocks, n, k)
     groups, pairs = 2, 2
-    assert packed.size == oracle_mod.packed_size(n, k) == groups * pairs * 4 * 576
-    rec = packed.reshape(groups, pairs, 4, 576)
+    assert packed.size == oracle_mod.packed_size(n, k) == groups * pairs * 4608
+    rec = packed.reshape(groups, pairs, 4608)
     nb = k // 32
     seen = np.zeros(packed.size, dtype=np.int32)
-    for row in range(groups * 64):
+    for row in range(groups * 128):
         for blk in range(pairs * 2):
-            (G, p, t), _, _ = _locate(row, blk, 0)
-            r16 = row % 16
-            s = (r16 % 8) * 4 + (blk % 2) * 2 + r16 // 8
-            dbits = rec[G, p, t, 2 * s] | (rec[G, p, t, 2 * s + 1].astype(np.int64) << 8)
+            (G, p), _, _ = _locate(row, blk, 0)
+            r = row % 128
+            off = 4 * r + 2 * (blk % 2)
+            dbits = rec[G, p, off] | (rec[G, p, off + 1].astype(np.int64) << 8)
             real = row < n and blk < nb
             want_d = (blocks[row, blk, 0] | (blocks[row, blk, 1].astype(np.int64) << 8)) if real else 0
             assert dbits == want_d
             for elem in range(32):
-                (G, p, t), off, shift = _locate(row, blk, elem)
-                q = (rec[G, p, t, off] >> shift) & 0xF
+                (G, p), off, shift = _locate(row, blk, elem)
+                q = (rec[G, p, off] >> shift) & 0xF
                 if real:
                     src = blocks[row, blk, 2 + elem % 16]
                     want = (src & 0xF) if elem < 16 else (src >> 4)
                 else:
                     want = 8
                 assert q == want, (row, blk, elem)
-                seen[((G * pairs + p) * 4 + t) * 576 + off] += 1
+                seen[(G * pairs + p) * 4608 + off] += 1
     # every nibble byte is hit exactly twice (low and high nibble)
-    nib_bytes = np.concatenate([np.arange(64, 576) + r * 576 for r in range(groups * pairs * 4)])
+    nib_bytes = np.concatenate([np.arange(512, 4608) + r * 4608 for r in range(groups * pairs)])
     assert np.all(seen[nib_bytes] == 2)
