@@ -195,8 +195,8 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
 /* Profiling builds only (compiled with -DQ4MM_TRACE): kernels launched after
  * the call write 16-byte event records {globaltimer ns, event << 16 | warp
  * << 8 | lane, argument} for the CTA with blockIdx.x == cta into `buffer`
- * (device memory, 16-byte aligned, zeroed by the caller), split into 64
- * equal regions, one per recording thread (lanes 0..3 of warps 0..15); a
+ * (device memory, 16-byte aligned, zeroed by the caller), split into 96
+ * equal regions, one per recording thread (lanes 0..3 of warps 0..23); a
  * zero timestamp ends a region. NULL switches tracing off. Normal builds
  * return Q4_ERR_INVALID_ARG. */
 Q4MM_API int q4_debug_set_trace(void *buffer, size_t bytes, uint32_t cta);

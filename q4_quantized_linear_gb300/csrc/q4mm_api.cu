@@ -412,7 +412,7 @@ Q4MM_API int q4_debug_set_trace(void *buffer, size_t bytes, uint32_t cta)
     }
     if (!aligned(buffer, 16)) return Q4_ERR_ALIGNMENT;
     g_trace.buf = static_cast<unsigned long long *>(buffer);
-    g_trace.cap = static_cast<unsigned>(bytes / 16 / 64); // 64 regions
+    g_trace.cap = static_cast<unsigned>(bytes / 16 / kTraceRegions);
     g_trace.cta = cta;
     return Q4_OK;
 #else

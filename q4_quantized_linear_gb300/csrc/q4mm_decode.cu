@@ -6,29 +6,39 @@
 // cost what one did on the card) and goinfer ch. 10 ("What the kernels are")
 // calls the quantised GEMV the decode workhorse.
 //
-// Design (GB300, one kernel per call and K range):
-//   * A CTA owns 128 weight rows (one packed group) and a slice of K; the
-//     slices of a group form one thread-block cluster (up to 8 CTAs).
-//   * Warp 0: four producer lanes, each owning every fourth pair, stream the
-//     4608-byte packed records through a shared-memory ring with 1-D bulk
-//     copies (several independent rings keep tens of KB in flight per SM).
-//   * Warps 2-9: each thread owns one weight row; it turns the pair's 64
-//     split-half nibbles into fp16 (q - 8) * d, rounded once, and stores them
-//     straight into tensor memory (tcgen05.st). No warp waits on a tensor
-//     core result, so the CUDA cores only stream.
-//   * Warp 1: one thread issues tcgen05.mma kind::f16: A = those weights
-//     from tensor memory, B = X from shared memory, D = 128 x N fp32 in
-//     tensor memory.
-//   * Warps 10-13 stage X once per CTA while the first weights stream and
-//     dequantise: every token row is scaled by a power of two (its largest
-//     |x| in the slice lands in [2^14, 2^15)) and split into fp16 hi + lo,
-//     22 significant bits, as the N = 16 (m <= 8) or N = 32 rows of the B
-//     operand. They then run the epilogue.
-//   * Epilogue: y = (D_hi + D_lo) / scale. Slices of a cluster add their
-//     partial rows into the first CTA's shared memory (DSMEM) and that CTA
-//     sums them in slice order, so results are bitwise reproducible and no
-//     global scratch is needed. K ranges too long for one cluster run as
-//     further launches that add into Y in order.
+// Design (GB300): one persistent launch per call and K range.
+//   * Work is split into 128-row groups (one packed group each) and S slices
+//     of K. The S CTAs of a thread-block cluster hold the S slices and walk
+//     the groups c, c + C, c + 2C, ... of their cluster c together, so each
+//     CTA stages its slice of X once and streams weight records without a
+//     break from one group to the next. Two CTAs fit on an SM.
+//   * Warp 0: four producer lanes, each owning every fourth record of the
+//     CTA's sequence, stream the 4608-byte packed records through a shared-
+//     memory ring with 1-D bulk copies.
+//   * Warps 3-10, two sets of four (one warp per TMEM sub-partition): each
+//     thread owns one weight row; it turns a pair's 64 split-half nibbles into
+//     fp16 (q - 8) * d, rounded once, and stores them straight into tensor
+//     memory (tcgen05.st). The sets take alternate records.
+//   * Warps 1-2: one thread each issues tcgen05.mma kind::f16 for every other
+//     pair of a group into its own accumulator: A = those weights from tensor
+//     memory, B = X from shared memory, D = 128 x N fp32 in tensor memory. A
+//     single issuing warp can start an MMA only every ~50 cycles, whatever N
+//     is; two keep the four MMAs of a pair well inside its HBM time. The
+//     accumulators are double-buffered across groups.
+//   * Warps 11-14 stage X: every token row is scaled by a power of two (its
+//     largest |x| in the slice lands in [2^14, 2^15)) and split into fp16 hi
+//     + lo, 22 significant bits, as the N = 16 (m <= 8) or N = 32 rows of the
+//     B operand. They then drain each group's accumulators while the next
+//     group streams: y = ((D0_hi + D0_lo) + (D1_hi + D1_lo)) / scale.
+//   * Slices meet in the first CTA of the cluster: the others store their
+//     partial rows into its shared memory (DSMEM) and signal an mbarrier
+//     there; it sums them in slice order and writes Y, so results are
+//     bitwise reproducible and no global scratch is needed. K ranges too long
+//     for one cluster run as further launches that add into Y in order.
+//   * Only the X warps wait for the preceding kernel (griddepcontrol.wait);
+//     with weights declared read-only the producer streams, and the
+//     dequantisers convert, before it has finished, and every CTA lets the
+//     next kernel be scheduled as soon as it has started.
 #include <algorithm>
 #include <cuda_runtime.h>
 
@@ -39,17 +49,33 @@ namespace q4 {
 namespace {
 
 constexpr int kErrTimeout = 5; // Q4_ERR_DEVICE_TIMEOUT
-constexpr int kDequantWarps = 8;
+constexpr int kIssuers = 2;         // MMA-issuing warps, one accumulator each
 constexpr int kXWarps = 4;          // stage X, then the epilogue (one per TMEM sub-partition)
-constexpr int kXWarp0 = 2 + kDequantWarps;
+constexpr int kDeqWarp0 = 1 + kIssuers;
 constexpr int kXThreads = kXWarps * 32;
-constexpr int kThreads = (2 + kDequantWarps + kXWarps) * 32;
+
+// Warp layout for SETS dequantiser sets (records u = set (mod SETS)), four
+// warps each, one per TMEM sub-partition.
+template <int SETS>
+struct Warps {
+    static constexpr int kXWarp0 = kDeqWarp0 + 4 * SETS;
+    static constexpr int kThreads = (kXWarp0 + kXWarps) * 32;
+};
 constexpr int kProducerLanes = 4;
-constexpr int kAStages = 7;        // weight stages in tensor memory (32 columns each)
-constexpr int kAcol0 = 32;         // D uses columns 0..31
+constexpr int kMaxRing = 12;        // weight records in flight per CTA (deeper only queues)
 constexpr uint32_t kTmemCols = 256;
-constexpr int kStageUnroll = 4;
+constexpr int kLoadBatch = 2;       // staging items (two float4 each) a thread keeps in flight
 constexpr int kMaxSlices = 8;
+
+// Tensor-memory map for MMA width N: accumulators [group parity][issuer]
+// (N columns each), then dequantised weight stages of 32 columns.
+template <int N>
+struct Tmem {
+    static constexpr int kDCols = 2 * kIssuers * N;
+    static constexpr int kAcol0 = kDCols;
+    static constexpr int kAStages = (static_cast<int>(kTmemCols) - kDCols) / 32;
+    static_assert(kAStages >= 2 && kAStages % kIssuers == 0, "tensor memory layout");
+};
 
 // X image: per pair, N rows (hi tokens, then lo tokens) x 128 bytes, 128-byte
 // swizzle, chunk c = 4 blk + quad holding block elements 4 quad + {0,2,16,18,
@@ -72,43 +98,47 @@ __device__ __forceinline__ void split_f16(float xs, uint32_t &hi, uint32_t &lo)
     lo = isfinite(r) ? f16_bits(r) : 0u;
 }
 
-// One row's pair of blocks -> 32 fp16x2 columns of tensor memory (same
-// column order as the X image): (q - 8) exact, times d, rounded once.
-__device__ __forceinline__ void dequant_pair_f16(uint32_t d01, uint4 q0, uint4 q1, uint32_t out[32])
+// One row's block -> 16 fp16x2 columns of tensor memory (same column order
+// as the X image): (q - 8) exact, times d, rounded once.
+__device__ __forceinline__ void dequant_block_f16(uint32_t dbits, uint4 q, uint32_t out[16])
 {
+    const uint32_t dd = dbits | (dbits << 16);
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-        const uint32_t h = blk ? (d01 >> 16) : (d01 & 0xFFFFu);
-        const uint32_t dd = h | (h << 16);
-        const uint4 q = blk ? q1 : q0;
-        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+    for (int wd = 0; wd < 4; ++wd) {
+        uint32_t v[4];
+        unpack_word_f16(words[wd], v);
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-            uint32_t v[4];
-            unpack_word_f16(words[wd], v);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) out[blk * 16 + wd * 4 + j] = hmul2_bits(v[j], dd);
-        }
+        for (int j = 0; j < 4; ++j) out[wd * 4 + j] = hmul2_bits(v[j], dd);
     }
 }
 
 struct Smem {
     uint8_t *xs, *w;
-    float *red;
-    uint64_t *full_w, *empty_w, *full_a, *empty_a, *done, *x_ready;
+    float *red;           // [2][S - 1][m][128] partial rows (first CTA of the cluster)
+    uint64_t *full_w, *empty_w, *full_a, *empty_a;
+    uint64_t *dfull, *dfree;       // [2] accumulators of a group parity ready / drained
+    uint64_t *red_full, *red_free; // [2] partials landed (first CTA) / slot free (others)
+    uint64_t *x_ready;
     uint32_t *tmem_slot;
-    int *abort;
     unsigned *maxbits;    // [16] largest |x| bits per token
     float *scale_up;      // [16] 2^e per token
     float *scale_dn;      // [16] 2^-e per token
+    int *rowid;           // [16] X / Y row of each token
 };
 
-__device__ __forceinline__ bool aborted(const Smem &sm) { return *reinterpret_cast<volatile int *>(sm.abort) != 0; }
+__device__ __forceinline__ void fail(const DecodeArgs &a) { record_status(a.status, kErrTimeout); }
 
-__device__ __forceinline__ void fail(const Smem &sm, const DecodeArgs &a)
+// Bounded wait by every lane of a warp, with one outcome for the whole warp,
+// so that a timeout never leaves a warp diverged in front of the .aligned
+// tcgen05 instructions that follow.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
-    *reinterpret_cast<volatile int *>(sm.abort) = 1;
-    record_status(a.status, kErrTimeout);
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, limit_ns)) != 0;
+}
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    return __all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar, parity, limit_ns)) != 0;
 }
 
 __device__ __forceinline__ void xwarps_sync()
@@ -116,40 +146,105 @@ __device__ __forceinline__ void xwarps_sync()
     asm volatile("bar.sync 2, %0;" ::"n"(kXThreads) : "memory");
 }
 
-// Stage the slice of X (pairs p0 .. p0+P-1) as the scaled fp16 hi/lo image.
-// Run by the kXThreads threads of the X warps; xt is the thread's index among
-// them.
+// Zero the token rows of the X image that no token fills (m < N / 2). Needs
+// nothing from the preceding kernel, so it runs before the dependency wait.
 template <int N>
-__device__ __forceinline__ void stage_x(const DecodeArgs &a, const Smem &sm, int p0, int P, int xt)
+__device__ __forceinline__ void zero_x_padding(const Smem &sm, int m, int P, int xt)
+{
+    constexpr int MP = N / 2;
+    const int pad = MP - m;     // padded rows per half
+    if (pad <= 0) return;
+    const int per_pair = 2 * pad * 8;
+    for (int i = xt; i < P * per_pair; i += kXThreads) {
+        const int q = i / per_pair, r = i - q * per_pair;
+        const int half = r / (pad * 8), rr = r - half * pad * 8;
+        const int row = half * MP + m + (rr >> 3);
+        sts128(sm.xs + q * N * 128 + row * 128 + (rr & 7) * 16, make_uint4(0u, 0u, 0u, 0u));
+    }
+}
+
+// Loads of one staging item: token t, pair q, chunk c (block c >> 2, quad
+// c & 3) = block elements 4 quad .. 4 quad + 3 and 16 + 4 quad .. + 3.
+__device__ __forceinline__ void load_item(const DecodeArgs &a, const Smem &sm, int p0, int it, float4 &xa, float4 &xb)
+{
+    const int m = a.m;
+    const int c = it & 7, t = (it >> 3) % m, q = (it >> 3) / m;
+    const int b = 2 * (p0 + q) + (c >> 2);
+    xa = make_float4(0.f, 0.f, 0.f, 0.f);
+    xb = xa;
+    if (b < a.nb) {
+        const float *xr = a.X + static_cast<int64_t>(sm.rowid[t]) * a.ldx + 32 * b + 4 * (c & 3);
+        xa = __ldg(reinterpret_cast<const float4 *>(xr));
+        xb = __ldg(reinterpret_cast<const float4 *>(xr + 16));
+    }
+}
+
+__device__ __forceinline__ unsigned absmax_bits(const float4 &v)
+{
+    return max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+               max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu));
+}
+
+template <int N>
+__device__ __forceinline__ void store_item(const DecodeArgs &a, const Smem &sm, int it, const float4 &xa, const float4 &xb)
 {
     constexpr int MP = N / 2;
     const int m = a.m;
-    const int lane = xt & 31;
-    const int kslice = P * 64;
-    const int64_t col0 = static_cast<int64_t>(p0) * 64;
-    const int64_t kreal = static_cast<int64_t>(a.nb) * 32;
+    const int c = it & 7, t = (it >> 3) % m, q = (it >> 3) / m;
+    const float su = sm.scale_up[t];
+    const float v[8] = {xa.x, xa.z, xb.x, xb.z, xa.y, xa.w, xb.y, xb.w};
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h0, l0, h1, l1;
+        split_f16(v[2 * i] * su, h0, l0);
+        split_f16(v[2 * i + 1] * su, h1, l1);
+        hw[i] = h0 | (h1 << 16);
+        lw[i] = l0 | (l1 << 16);
+    }
+    sts128(sm.xs + ximg_off(N, q, t, c), make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(sm.xs + ximg_off(N, q, MP + t, c), make_uint4(lw[0], lw[1], lw[2], lw[3]));
+}
+
+// Stage the slice of X (pairs p0 .. p0+P-1) as the scaled fp16 hi/lo image.
+// Run by the kXThreads threads of the X warps after the dependency wait; xt
+// is the thread's index among them. The first kLoadBatch items of every
+// thread stay in registers between the two passes, so a slice of up to
+// kXThreads * kLoadBatch items costs one round trip to memory.
+template <int N>
+__device__ __forceinline__ void stage_x(const DecodeArgs &a, const Smem &sm, int p0, int P, int xt, const TraceRef &tr)
+{
+    const int m = a.m;
+    if (xt < m) sm.rowid[xt] = a.rows ? a.rows[xt] : xt;
+    xwarps_sync();
+    const int items = P * m * 8;
     // 1. largest |x| of each token over the slice
-    for (int t = 0; t < m; ++t) {
-        const int64_t row = a.rows ? static_cast<int64_t>(a.rows[t]) : t;
-        const float *xr = a.X + row * a.ldx + col0;
-        unsigned mx = 0;
-        for (int i = xt; i < kslice / 4; i += kXThreads) {
-            if (col0 + 4 * i < kreal) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(xr) + i);
-                mx = max(mx, max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
-                                 max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu)));
-            }
+    float4 ra[kLoadBatch], rb[kLoadBatch];
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+        const int it = xt + u * kXThreads;
+        if (it < items) load_item(a, sm, p0, it, ra[u], rb[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoadBatch; ++u) {
+        const int it = xt + u * kXThreads;
+        if (it < items) atomicMax(&sm.maxbits[(it >> 3) % m], max(absmax_bits(ra[u]), absmax_bits(rb[u])));
+    }
+    for (int base = xt + kLoadBatch * kXThreads; base < items; base += kLoadBatch * kXThreads) {
+        float4 va[kLoadBatch], vb[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int it = base + u * kXThreads;
+            if (it < items) load_item(a, sm, p0, it, va[u], vb[u]);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        if (lane == 0) atomicMax(&sm.maxbits[t], mx);
-    }
-    // zero the image (padded token rows and padded K stay zero)
-    if (m < MP) {
-        const int vecs = P * N * 8;
-        for (int i = xt; i < vecs; i += kXThreads) sts128(sm.xs + i * 16, make_uint4(0u, 0u, 0u, 0u));
+        for (int u = 0; u < kLoadBatch; ++u) {
+            const int it = base + u * kXThreads;
+            if (it < items) atomicMax(&sm.maxbits[(it >> 3) % m], max(absmax_bits(va[u]), absmax_bits(vb[u])));
+        }
     }
     xwarps_sync();
+    if (xt == 0) trace(tr, kTrXLoaded, 0);
     // 2. per-token power of two: largest |x| into [2^14, 2^15)
     if (xt < m) {
         const unsigned mb = sm.maxbits[xt];
@@ -163,46 +258,24 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const Smem &sm, int
         sm.scale_dn[xt] = __uint_as_float(static_cast<unsigned>(127 - e) << 23);
     }
     xwarps_sync();
-    // 3. the split, item = (pair q, token t, chunk c); loads of kStageUnroll
-    //    items in flight per thread
-    const int items = P * m * 8;
-    for (int base = xt; base < items; base += kXThreads * kStageUnroll) {
-        float4 xa[kStageUnroll], xb[kStageUnroll];
+    if (xt == 0) trace(tr, kTrXScaled, 0);
+    // 3. the split: first batch from registers, the rest reloaded (L1 hits)
 #pragma unroll
-        for (int u = 0; u < kStageUnroll; ++u) {
+    for (int u = 0; u < kLoadBatch; ++u) {
+        const int it = xt + u * kXThreads;
+        if (it < items) store_item<N>(a, sm, it, ra[u], rb[u]);
+    }
+    for (int base = xt + kLoadBatch * kXThreads; base < items; base += kLoadBatch * kXThreads) {
+        float4 va[kLoadBatch], vb[kLoadBatch];
+#pragma unroll
+        for (int u = 0; u < kLoadBatch; ++u) {
             const int it = base + u * kXThreads;
-            xa[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            xb[u] = xa[u];
-            if (it < items) {
-                const int c = it & 7, t = (it >> 3) % m, q = (it >> 3) / m;
-                const int b = 2 * (p0 + q) + (c >> 2);
-                if (b < a.nb) {
-                    const int64_t row = a.rows ? static_cast<int64_t>(a.rows[t]) : t;
-                    const float *xr = a.X + row * a.ldx + 32 * b + 4 * (c & 3);
-                    xa[u] = __ldg(reinterpret_cast<const float4 *>(xr));
-                    xb[u] = __ldg(reinterpret_cast<const float4 *>(xr + 16));
-                }
-            }
+            if (it < items) load_item(a, sm, p0, it, va[u], vb[u]);
         }
 #pragma unroll
-        for (int u = 0; u < kStageUnroll; ++u) {
+        for (int u = 0; u < kLoadBatch; ++u) {
             const int it = base + u * kXThreads;
-            if (it < items) {
-                const int c = it & 7, t = (it >> 3) % m, q = (it >> 3) / m;
-                const float su = sm.scale_up[t];
-                const float v[8] = {xa[u].x, xa[u].z, xb[u].x, xb[u].z, xa[u].y, xa[u].w, xb[u].y, xb[u].w};
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t h0, l0, h1, l1;
-                    split_f16(v[2 * i] * su, h0, l0);
-                    split_f16(v[2 * i + 1] * su, h1, l1);
-                    hw[i] = h0 | (h1 << 16);
-                    lw[i] = l0 | (l1 << 16);
-                }
-                sts128(sm.xs + ximg_off(N, q, t, c), make_uint4(hw[0], hw[1], hw[2], hw[3]));
-                sts128(sm.xs + ximg_off(N, q, MP + t, c), make_uint4(lw[0], lw[1], lw[2], lw[3]));
-            }
+            if (it < items) store_item<N>(a, sm, it, va[u], vb[u]);
         }
     }
     // generic-proxy writes -> visible to the tensor core's shared-memory reads
@@ -211,20 +284,31 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const Smem &sm, int
     if (xt == 0) mbar_arrive(sm.x_ready);
 }
 
-template <int N>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
+// Every barrier of the pipeline has a single waiter agent that sees all of
+// its phases in order (a parity wait is only sound that way): ring slot s is
+// always refilled by producer lane s % 4 and drained by set s % SETS (the
+// ring depth is a multiple of both), and stage s is always written by set
+// s % SETS and read by issuer s % 2 (the stage count is a multiple of both).
+template <int N, int SETS>
+__global__ void __launch_bounds__(Warps<SETS>::kThreads, 2) decode_kernel(const DecodeArgs a)
 {
     constexpr int MP = N / 2;
+    constexpr int AS = Tmem<N>::kAStages;
+    constexpr int kAcol0 = Tmem<N>::kAcol0;
+    constexpr int kXWarp0 = Warps<SETS>::kXWarp0;
+    static_assert(AS % SETS == 0, "a stage must always belong to one dequantiser set");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = a.S;
     const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int G = blockIdx.x / S;                   // 128-row group
+    const int G0 = blockIdx.x / S;                  // first group of this cluster
+    const int stride = a.clusters;
+    const int ntiles = G0 < a.groups ? (a.groups - 1 - G0) / stride + 1 : 0;
     const int p0 = a.pass_p0 + rank * a.pbase + min(rank, a.prem);
     const int P = a.pbase + (rank < a.prem ? 1 : 0);
-    const int R = a.ring;
+    const int total = ntiles * P;                    // records this CTA streams
     const int m = a.m;
     const TraceRef tr{a.trace_buf, a.trace_cap, a.trace_cta};
     trace_init();
@@ -233,177 +317,259 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     Smem sm;
     sm.xs = base;
     sm.w = sm.xs + a.xs_bytes;
+    const int R = a.ring;
     sm.red = reinterpret_cast<float *>(sm.w + static_cast<size_t>(R) * kRecordBytes);
-    const int red_floats = S > 1 ? (S - 1) * m * 128 : 0;
+    const int red_floats = S > 1 ? 2 * (S - 1) * m * 128 : 0;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm.red + red_floats + (red_floats & 1));
     sm.full_w = bars;
     sm.empty_w = sm.full_w + R;
     sm.full_a = sm.empty_w + R;
-    sm.empty_a = sm.full_a + kAStages;
-    sm.done = sm.empty_a + kAStages;
-    sm.x_ready = sm.done + 1;
+    sm.empty_a = sm.full_a + AS;
+    sm.dfull = sm.empty_a + AS;
+    sm.dfree = sm.dfull + 2;
+    sm.red_full = sm.dfree + 2;
+    sm.red_free = sm.red_full + 2;
+    sm.x_ready = sm.red_free + 2;
     sm.tmem_slot = reinterpret_cast<uint32_t *>(sm.x_ready + 1);
-    sm.abort = reinterpret_cast<int *>(sm.tmem_slot + 1);
-    sm.maxbits = reinterpret_cast<unsigned *>(sm.abort + 1);
+    sm.maxbits = reinterpret_cast<unsigned *>(sm.tmem_slot + 1);
     sm.scale_up = reinterpret_cast<float *>(sm.maxbits + 16);
     sm.scale_dn = sm.scale_up + 16;
+    sm.rowid = reinterpret_cast<int *>(sm.scale_dn + 16);
 
     if (tid == 0) {
-        for (int i = 0; i < R; ++i) mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], kDequantWarps / 2);
-        for (int i = 0; i < kAStages; ++i) mbar_init(&sm.full_a[i], kDequantWarps / 2), mbar_init(&sm.empty_a[i], 1);
-        mbar_init(sm.done, 1);
+        for (int i = 0; i < R; ++i) mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], 4);
+        for (int i = 0; i < AS; ++i) mbar_init(&sm.full_a[i], 4), mbar_init(&sm.empty_a[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.dfull[i], kIssuers);
+            mbar_init(&sm.dfree[i], kXWarps);
+            mbar_init(&sm.red_full[i], S > 1 ? kXWarps * (S - 1) : 1);
+            mbar_init(&sm.red_free[i], kXWarps);
+        }
         mbar_init(sm.x_ready, 1);
-        *sm.abort = 0;
         fence_barrier_init();
     }
     if (tid < 16) sm.maxbits[tid] = 0u;
     if (warp == 1) {
         tmem_alloc(sm.tmem_slot, kTmemCols);
         tmem_relinquish();
+        if (lane == 0) trace(tr, kTrAlloc, 0);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (S > 1) cluster_sync(); // every CTA of the cluster is running before any DSMEM traffic
+    // The next kernel in the stream may be scheduled now: it waits for this
+    // one to complete before it reads anything this one writes.
+    pdl_launch_dependents();
+    if (tid == 0) trace(tr, kTrSetup, 0);
+    if (S > 1) cluster_sync(); // barriers of every CTA initialised before any remote arrive
     const uint32_t tmem = *sm.tmem_slot;
-
-    const uint8_t *wsrc = a.W + (static_cast<int64_t>(G) * a.np + p0) * kRecordBytes;
-    const bool producer = warp == 0 && lane < kProducerLanes;
-    const uint64_t pol = policy_evict_first();
-    int w_next = lane; // producer lane: next pair (relative to p0) to issue
-    auto issue = [&](int j) {
-        const int s = j % R;
-        trace(tr, kTrWIssue, static_cast<unsigned>(j));
-        mbar_arrive_expect_tx(&sm.full_w[s], kRecordBytes);
-        bulk_g2s_hint(sm.w + static_cast<size_t>(s) * kRecordBytes, wsrc + static_cast<size_t>(j) * kRecordBytes,
-                      kRecordBytes, &sm.full_w[s], pol);
-    };
-
-    // Weights may stream before the preceding kernel has finished only when
-    // the caller declared them read-only; X and Y are touched after the wait.
-    if (producer && a.prefetch_w)
-        for (; w_next < P && w_next < R; w_next += kProducerLanes) issue(w_next);
-    pdl_wait();
-    if (tid == 0) trace(tr, kTrPdl, 0);
-    if (producer)
-        for (; w_next < P && w_next < R; w_next += kProducerLanes) issue(w_next);
+    if (tid == 0) trace(tr, kTrSetup, 1);
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (producer) {
-            int last = w_next - kProducerLanes;
-            for (int j = w_next; j < P && !aborted(sm); j += kProducerLanes) {
-                if (!mbar_wait(&sm.empty_w[j % R], ((j / R) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
-                issue(j);
-                last = j;
+        // Weights may stream before the preceding kernel has finished only
+        // when the caller declared them read-only.
+        if (!a.prefetch_w) pdl_wait();
+        if (lane < kProducerLanes && total > 0) {
+            const uint64_t pol = policy_evict_first();
+            // record u = lane, lane + 4, ...: group i, pair j, ring slot s
+            int i = 0, j = lane, s = lane, last = -1;
+            uint32_t ph = 0;
+            while (j >= P) j -= P, ++i;
+            for (int u = lane; u < total; u += kProducerLanes) {
+                if (u >= R && !mbar_wait(&sm.empty_w[s], ph ^ 1u, a.wait_ns)) { fail(a); break; }
+                trace(tr, kTrWIssue, static_cast<unsigned>(u));
+                const int64_t rec = static_cast<int64_t>(G0 + i * stride) * a.np + p0 + j;
+                mbar_arrive_expect_tx(&sm.full_w[s], kRecordBytes);
+                bulk_g2s_hint(sm.w + static_cast<size_t>(s) * kRecordBytes, a.W + rec * kRecordBytes, kRecordBytes,
+                              &sm.full_w[s], pol);
+                last = u;
+                s += kProducerLanes;
+                if (s >= R) s -= R, ph ^= 1u;
+                j += kProducerLanes;
+                while (j >= P) j -= P, ++i;
             }
-            for (int j = last; j >= 0 && j > last - R; j -= kProducerLanes)
-                if (!mbar_wait(&sm.full_w[j % R], (j / R) & 1, a.wait_ns)) fail(sm, a);
+            // No copy of ours may still be landing when the CTA exits. A record
+            // whose slot a later record reused has landed (and been consumed)
+            // already; only the last R records of the sequence need a wait.
+            for (int u = last; u >= 0 && u >= total - R; u -= kProducerLanes)
+                if (!mbar_wait(&sm.full_w[u % R], (u / R) & 1, a.wait_ns)) fail(a);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp < kDeqWarp0) {
         // --------------------------------------------------------------- MMA
+        // Issuer e owns the records u = e (mod kIssuers) -- in group i the
+        // pairs j = e + i P (mod 2) -- and the accumulator [group parity][e].
+        // Descriptor arithmetic is hoisted so the four MMAs of a pair issue
+        // back to back.
+        const int e = warp - 1;
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(128, N);
-            const uint32_t xs0 = smem_u32(sm.xs);
-            if (P > 0 && !mbar_wait(sm.x_ready, 0, a.wait_ns)) fail(sm, a);
-            for (int j = 0; j < P && !aborted(sm); ++j) {
-                const int sa = j % kAStages;
-                if (!mbar_wait(&sm.full_a[sa], (j / kAStages) & 1, a.wait_ns)) { fail(sm, a); break; }
-                trace(tr, kTrMmaIssue, static_cast<unsigned>(j));
-                tc_fence_after();
-                const uint32_t at = tmem + kAcol0 + static_cast<uint32_t>(sa) * 32u;
-                const uint32_t bs = xs0 + static_cast<uint32_t>(j * N * 128);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_f16_ts(tmem, at + 8 * kk, smem_desc_sw128(bs + kk * 32), idesc, (j | kk) != 0);
-                tc_commit(&sm.empty_a[sa]);
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sm.xs));
+            constexpr uint64_t kPairStep = static_cast<uint64_t>((N * 128) >> 4);
+            bool ok = ntiles == 0 || mbar_wait(sm.x_ready, 0, a.wait_ns);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int tb = i & 1;
+                const int j0 = (e + i * P) & 1;
+                if (j0 < P) {
+                    if (i >= 2 && !mbar_wait(&sm.dfree[tb], ((i >> 1) & 1) ^ 1, a.wait_ns)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + static_cast<uint32_t>((tb * kIssuers + e) * N);
+                    uint64_t bdesc = bdesc0 + kPairStep * static_cast<uint64_t>(j0);
+                    uint32_t acc = 0;
+                    for (int j = j0; j < P; j += kIssuers) {
+                        const int u = i * P + j;
+                        const int sa = u % AS;
+                        if (!mbar_wait(&sm.full_a[sa], (u / AS) & 1, a.wait_ns)) { ok = false; break; }
+                        trace(tr, kTrMmaIssue, static_cast<unsigned>(u));
+                        tc_fence_after();
+                        const uint32_t at = tmem + static_cast<uint32_t>(kAcol0 + sa * 32);
+                        tc_mma_f16_ts(d_tmem, at, bdesc, idesc, acc);
+                        tc_mma_f16_ts(d_tmem, at + 8u, bdesc + 2u, idesc, 1u);
+                        tc_mma_f16_ts(d_tmem, at + 16u, bdesc + 4u, idesc, 1u);
+                        tc_mma_f16_ts(d_tmem, at + 24u, bdesc + 6u, idesc, 1u);
+                        tc_commit(&sm.empty_a[sa]);
+                        acc = 1u;
+                        bdesc += kIssuers * kPairStep;
+                    }
+                    if (!ok) break;
+                }
+                tc_commit(&sm.dfull[tb]); // the group's MMAs of this issuer are done (at once if it had none)
             }
-            tc_commit(sm.done); // also taken on abort: no MMA of ours is in flight past this
+            // The tensor core's arrivals on the stage barriers must all have
+            // landed before the CTA exits: wait for the last use of each stage.
+            if (ok && e == 0)
+                for (int st = 0; st < AS && st < total; ++st) {
+                    const int u = st + AS * ((total - 1 - st) / AS);
+                    if (!mbar_wait(&sm.empty_a[st], (u / AS) & 1, a.wait_ns)) { ok = false; break; }
+                }
+            if (!ok) fail(a);
         }
         __syncwarp();
-    } else if (warp >= kXWarp0) {
-        // ------------------------------------------------------------ stage X
-        stage_x<N>(a, sm, p0, P, tid - kXWarp0 * 32);
-        if (tid == kXWarp0 * 32) trace(tr, kTrXStaged, 0);
-    } else {
+    } else if (warp < kXWarp0) {
         // -------------------------------------------------------- dequantise
-        const int dw = warp - 2;
-        const int q = warp & 3;
+        // Set h converts records u = h (mod SETS), one block at a time.
+        const int dw = warp - kDeqWarp0;
+        const int q = warp & 3;              // TMEM sub-partition this warp may access
         const int h = dw >> 2;
         const int row = q * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        for (int j = h; j < P && !aborted(sm); j += 2) {
-            const int sw = j % R, sa = j % kAStages;
-            if (!mbar_wait(&sm.full_w[sw], (j / R) & 1, a.wait_ns)) { fail(sm, a); break; }
-            if (lane == 0) trace(tr, kTrWFull, static_cast<unsigned>(j));
-            if (!mbar_wait(&sm.empty_a[sa], ((j / kAStages) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
+        int sw = h, sa = h;                  // ring slot and tensor-memory stage of record u
+        uint32_t phw = 0, pha = 0;
+        for (int u = h; u < total; u += SETS) {
+            if (!warp_wait(&sm.full_w[sw], phw, a.wait_ns)) { fail(a); break; }
+            if (lane == 0) trace(tr, kTrWFull, static_cast<unsigned>(u));
             const uint8_t *rec = sm.w + static_cast<size_t>(sw) * kRecordBytes;
             const uint32_t d01 = *reinterpret_cast<const uint32_t *>(rec + kRecScaleOff + 4 * row);
             const uint4 q0 = lds128(rec + kRecQs0Off + 16 * row);
             const uint4 q1 = lds128(rec + kRecQs1Off + 16 * row);
-            uint32_t out[32];
-            dequant_pair_f16(d01, q0, q1, out);
-            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + static_cast<uint32_t>(sa) * 32u, out);
+            uint32_t out[16];
+            dequant_block_f16(d01 & 0xFFFFu, q0, out);
+            if (u >= AS && !warp_wait(&sm.empty_a[sa], pha ^ 1u, a.wait_ns)) { fail(a); break; }
+            tc_fence_after();
+            const uint32_t ta = tmem + lane_base + static_cast<uint32_t>(kAcol0 + sa * 32);
+            tmem_st_32x32b_x16(ta, out);
+            dequant_block_f16(d01 >> 16, q1, out);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty_w[sw]);   // the record has been consumed
+            tmem_st_32x32b_x16(ta + 16u, out);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.full_a[sa]);
-                mbar_arrive(&sm.empty_w[sw]);
-                trace(tr, kTrDeqDone, static_cast<unsigned>(j));
+                trace(tr, kTrDeqDone, static_cast<unsigned>(u));
             }
+            sw += SETS;
+            if (sw >= R) sw -= R, phw ^= 1u;
+            sa += SETS;
+            if (sa >= AS) sa -= AS, pha ^= 1u;
         }
-    }
+    } else {
+        // ------------------------------------------------ stage X, epilogue
+        const int xt = tid - kXWarp0 * 32;
+        zero_x_padding<N>(sm, m, P, xt);
+        pdl_wait();
+        if (xt == 0) trace(tr, kTrPdl, 0);
+        stage_x<N>(a, sm, p0, P, xt, tr);
+        if (xt == 0) trace(tr, kTrXStaged, 0);
 
-    // ------------------------------------------------------------ epilogue
-    // the X warps cover the four TMEM sub-partitions: thread = weight row
-    const bool epi = warp >= kXWarp0;
-    const int q = warp & 3;
-    const int row = q * 32 + lane;
-    const int64_t grow = static_cast<int64_t>(G) * kGroupRows + row;
-    float y[MP];
+        // thread = weight row of the group, in this warp's TMEM sub-partition
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t red0 = smem_u32(sm.red);
+        for (int i = 0; i < ntiles; ++i) {
+            const int tb = i & 1;
+            const uint32_t par = static_cast<uint32_t>((i >> 1) & 1);
+            if (!warp_wait(&sm.dfull[tb], par, a.wait_ns)) { fail(a); break; }
+            tc_fence_after();
+            // y = (((D0_hi + D0_lo) + D1_hi) + D1_lo) * 2^-e, in this order;
+            // 8 columns per load (hi rows 0..MP-1, then lo rows)
+            float y[MP];
 #pragma unroll
-    for (int t = 0; t < MP; ++t) y[t] = 0.f;
-    if (epi) {
-        if (!mbar_wait(sm.done, 0, a.wait_ns)) fail(sm, a);
-        if (lane == 0) trace(tr, kTrDone, 0);
-        tc_fence_after();
-        uint32_t d[N];
-        if constexpr (N == 16) {
-            tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(q * 32) << 16), d);
-        } else {
-            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16), d);
-        }
-        tmem_wait_ld();
-        if (P > 0) {
+            for (int t = 0; t < MP; ++t) y[t] = 0.f;
+#pragma unroll
+            for (int e = 0; e < kIssuers; ++e) {
+                if (((e + i * P) & 1) >= P) continue;   // issuer e had no pair of this group
+#pragma unroll
+                for (int c0 = 0; c0 < N; c0 += 8) {
+                    uint32_t d[8];
+                    tmem_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>((tb * kIssuers + e) * N + c0), d);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int t = (c0 + c) % MP;
+                        if (t < m) y[t] += __uint_as_float(d[c]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.dfree[tb]);
 #pragma unroll
             for (int t = 0; t < MP; ++t)
-                if (t < m) y[t] = (__uint_as_float(d[t]) + __uint_as_float(d[MP + t])) * sm.scale_dn[t];
-        }
-        if (S > 1 && rank > 0) {
-            const uint32_t dst = mapa_shared(smem_u32(sm.red), 0u);
+                if (t < m) y[t] *= sm.scale_dn[t];
+
+            const int64_t grow = static_cast<int64_t>(G0 + i * stride) * kGroupRows + row;
+            if (rank > 0) {
+                // partial rows into the first CTA's slot tb, then signal it
+                if (i >= 2 && !warp_wait_cluster(&sm.red_free[tb], par ^ 1u, a.wait_ns)) { fail(a); break; }
+                const uint32_t dst = mapa_shared(red0, 0u) +
+                                     static_cast<uint32_t>((((tb * (S - 1) + rank - 1) * m) * 128 + row) * 4);
 #pragma unroll
-            for (int t = 0; t < MP; ++t)
-                if (t < m) st_cluster_f32(dst + static_cast<uint32_t>((((rank - 1) * m + t) * 128 + row) * 4), y[t]);
-        }
-    }
-    pdl_launch_dependents();
-    if (S > 1) cluster_sync(); // partial rows have landed in the first CTA
-    if (epi && rank == 0 && grow < a.n) {
+                for (int t = 0; t < MP; ++t)
+                    if (t < m) st_cluster_f32(dst + static_cast<uint32_t>(t * 128 * 4), y[t]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_full[tb]), 0u));
+            } else {
+                if (S > 1 && !warp_wait_cluster(&sm.red_full[tb], par, a.wait_ns)) { fail(a); break; }
+                if (grow < a.n) {
 #pragma unroll
-        for (int t = 0; t < MP; ++t) {
-            if (t < m) {
-                float v = y[t];
-                for (int rr = 1; rr < S; ++rr) v += sm.red[((rr - 1) * m + t) * 128 + row];
-                const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[t]) : t;
-                float *dst = a.Y + yrow * a.ldy + grow;
-                *dst = a.accumulate ? *dst + v : v;
+                    for (int t = 0; t < MP; ++t) {
+                        if (t < m) {
+                            float v = y[t];
+                            for (int r = 1; r < S; ++r) v += sm.red[((tb * (S - 1) + r - 1) * m + t) * 128 + row];
+                            float *dst = a.Y + static_cast<int64_t>(sm.rowid[t]) * a.ldy + grow;
+                            *dst = a.accumulate ? *dst + v : v;
+                        }
+                    }
+                }
+                if (S > 1) {
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int r = 1; r < S; ++r)
+                            mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_free[tb]), static_cast<uint32_t>(r)));
+                }
             }
+            if (lane == 0) trace(tr, kTrTile, static_cast<unsigned>(i));
         }
+        if (lane == 0) trace(tr, kTrEpiDone, 0);
     }
 
-    if (epi && lane == 0) trace(tr, kTrEpiDone, 0);
+    // every CTA of the cluster stays until the others are done with its
+    // shared memory and barriers
+    if (S > 1) cluster_sync();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -413,53 +579,76 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeArgs a)
     if (tid == 0) trace(tr, kTrEnd, 0);
 }
 
-size_t decode_smem(int N, int P, int ring, int S, int64_t m)
+size_t decode_smem(int N, int P, int S, int64_t m, int ring)
 {
+    const int as = N == 16 ? Tmem<16>::kAStages : Tmem<32>::kAStages;
     const size_t xs = static_cast<size_t>(round_up(static_cast<int64_t>(P) * N * 128, 1024));
-    const size_t red = S > 1 ? static_cast<size_t>(S - 1) * m * 128 * 4 + 8 : 0;
-    const size_t bars = static_cast<size_t>(2 * ring + 2 * kAStages + 2) * 8 + 16 + 48 * 4;
+    const size_t red = S > 1 ? static_cast<size_t>(2 * (S - 1)) * m * 128 * 4 + 8 : 0;
+    const size_t bars = static_cast<size_t>(2 * ring + 2 * as + 9) * 8 + 4 + 64 * 4;
     return 1024 + xs + static_cast<size_t>(ring) * kRecordBytes + red + bars;
 }
 
 } // namespace
 
-// Choose the cluster size S (K slices per 128-row group, at most 8) and the
-// number of launches over K: the busiest SM's pair count plus a per-CTA
-// start-up cost, with at most two CTAs per SM (tensor memory: 256 columns each).
+// Choose the cluster size S (K slices per 128-row group, at most 8), the
+// number of persistent clusters, the number of launches over K and the ring
+// depth. Two CTAs share an SM (shared and tensor memory are sized for that).
+// Cost, in record times of one SM's share of HBM: the busiest SM's records,
+// or one CTA's records at the rate a single CTA's ring sustains (kCtaRate of
+// the share at a ring of 8, in proportion to the ring), whichever is larger,
+// plus per-group and per-CTA overheads.
 bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan)
 {
-    if (m < 1 || m > 16) return false;
+    if (m < 1 || m > 16 || sm_count < 1) return false;
+    constexpr double kCtaRate = 0.6;
     const int N = m <= 8 ? 16 : 32;
-    const int64_t tiles = ceil_div(n, kGroupRows);
+    const int64_t groups = ceil_div(n, kGroupRows);
     const int64_t np = ceil_div(k, kPairK);
-    const int64_t xs_budget = 96 * 1024;
-    const int64_t pmax = xs_budget / (N * 128);
+    const size_t smem_max = kSmemPerSM / 2 - 1024 - 512;   // two CTAs per SM
+    const size_t smem_min = kSmemPerSM / 3 + 1024;          // never three (tensor memory)
     DecodePlan best;
     double best_cost = 1e300;
-    for (int S = 1; S <= kMaxSlices; ++S) {
-        if (S > np) break;
-        const int64_t passes = ceil_div(np, S * pmax);
-        const int64_t ppp = ceil_div(np, passes);          // pairs per pass
-        if (ppp < S) continue;
-        const int64_t P = ceil_div(ppp, S);
-        const int ring = 8;
-        size_t smem = decode_smem(N, static_cast<int>(P), ring, S, m);
-        // at most two resident CTAs per SM, so that tensor memory always suffices
-        smem = std::max<size_t>(smem, kSmemPerSM / 3 + 1024);
-        if (smem > kSmemOptIn) continue;
-        const int64_t units = tiles * S;
-        const int64_t per_sm = ceil_div(units, sm_count);
-        const double cost = static_cast<double>(passes) * per_sm * (static_cast<double>(P) + 6.0 + (S > 1 ? 2.0 : 0.0));
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best.N = N;
-            best.S = S;
-            best.passes = static_cast<int>(passes);
-            best.pairs_per_pass = static_cast<int>(ppp);
-            best.ring = ring;
-            best.ctas = static_cast<int>(units);
-            best.xs_bytes = static_cast<int>(round_up(P * N * 128, 1024));
-            best.smem = smem;
+    for (int S = 1; S <= kMaxSlices && S <= np; ++S) {
+        for (int64_t passes = 1; passes <= np; ++passes) {
+            const int64_t ppp = ceil_div(np, passes);        // pairs per pass
+            if (ppp < S) break;
+            const int64_t P = ceil_div(ppp, S);
+            // ring: a multiple of the four producer lanes and of the sets
+            auto fits = [&](int r) { return decode_smem(N, static_cast<int>(P), S, m, r) <= smem_max; };
+            int sets = 2, ring = 0;
+            if (N == 16 && fits(12)) {
+                sets = 3;
+                ring = 12;
+            } else {
+                for (int r = kMaxRing; r >= 4 && ring == 0; r -= 4)
+                    if (fits(r)) ring = r;
+            }
+            if (ring == 0) continue;                          // more passes: smaller slices
+            const size_t smem = std::max(decode_smem(N, static_cast<int>(P), S, m, ring), smem_min);
+            const int64_t clusters = std::min<int64_t>(groups, (2 * sm_count) / S);
+            if (clusters < 1) break;
+            const int64_t tiles_per = ceil_div(groups, clusters);
+            const int64_t ctas = clusters * S;
+            const double cta_pairs = static_cast<double>(tiles_per * P);
+            const double sm_pairs = (ctas > sm_count ? 2.0 : 1.0) * cta_pairs;
+            const double rate = std::min(1.0, kCtaRate * ring / 8.0);
+            const double stream = std::max({sm_pairs, cta_pairs / rate, static_cast<double>(groups * ppp) / sm_count});
+            const double cost = static_cast<double>(passes) *
+                                (stream + static_cast<double>(tiles_per) * (1.5 + (S > 1 ? 1.0 : 0.0)) + 6.0);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.N = N;
+                best.S = S;
+                best.passes = static_cast<int>(passes);
+                best.pairs_per_pass = static_cast<int>(ppp);
+                best.clusters = static_cast<int>(clusters);
+                best.ctas = static_cast<int>(ctas);
+                best.ring = ring;
+                best.sets = sets;
+                best.xs_bytes = static_cast<int>(round_up(P * N * 128, 1024));
+                best.smem = smem;
+            }
+            break;                                            // fewest passes that fit
         }
     }
     if (best.ctas == 0) return false;
@@ -469,8 +658,11 @@ bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan
 
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaStream_t s)
 {
-    const void *fn = plan.N == 16 ? reinterpret_cast<const void *>(&decode_kernel<16>)
-                                  : reinterpret_cast<const void *>(&decode_kernel<32>);
+    const void *fn = plan.N == 32  ? reinterpret_cast<const void *>(&decode_kernel<32, 2>)
+                     : plan.sets == 3 ? reinterpret_cast<const void *>(&decode_kernel<16, 3>)
+                                      : reinterpret_cast<const void *>(&decode_kernel<16, 2>);
+    const int threads = plan.sets == 3 ? Warps<3>::kThreads : Warps<2>::kThreads;
+    if (plan.N == 32 && plan.sets != 2) return cudaErrorInvalidValue;
     cudaError_t e = set_max_smem(fn, plan.smem);
     if (e != cudaSuccess) return e;
     for (int pass = 0; pass < plan.passes; ++pass) {
@@ -480,15 +672,16 @@ cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaSt
         a.S = plan.S;
         a.pbase = pp / plan.S;
         a.prem = pp % plan.S;
-        a.accumulate = pass > 0 ? 1 : 0;
+        a.clusters = plan.clusters;
         a.ring = plan.ring;
+        a.accumulate = pass > 0 ? 1 : 0;
         a.xs_bytes = plan.xs_bytes;
         const TraceSettings ts = trace_settings();
         a.trace_buf = ts.buf;
         a.trace_cap = ts.cap;
         a.trace_cta = ts.cta;
         void *kargs[] = {&a};
-        e = launch_pdl(fn, dim3(plan.ctas), dim3(kThreads), plan.smem, s, kargs, plan.S);
+        e = launch_pdl(fn, dim3(plan.ctas), dim3(threads), plan.smem, s, kargs, plan.S);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

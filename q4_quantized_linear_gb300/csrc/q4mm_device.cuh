@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "q4mm_internal.h"
+
 namespace q4 {
 
 // ----------------------------------------------------------------- basics --
@@ -38,13 +40,14 @@ struct TraceRef {
 
 enum TraceEvent : unsigned {
     kTrStart = 1, kTrPdl = 2, kTrXStaged = 3, kTrWIssue = 4, kTrWFull = 5, kTrDeqDone = 6,
-    kTrMmaIssue = 7, kTrBIssue = 8, kTrDone = 9, kTrEpiDone = 10, kTrEnd = 11, kTrBFull = 12
+    kTrMmaIssue = 7, kTrBIssue = 8, kTrDone = 9, kTrEpiDone = 10, kTrEnd = 11, kTrBFull = 12,
+    kTrSetup = 13, kTrTile = 14, kTrAlloc = 15, kTrXLoaded = 16, kTrXScaled = 17, kTrRed = 18
 };
 
 #ifdef Q4MM_TRACE
 __device__ __forceinline__ unsigned *trace_counters()
 {
-    __shared__ unsigned counters[64];
+    __shared__ unsigned counters[kTraceRegions];
     return counters;
 }
 #endif
@@ -53,7 +56,7 @@ __device__ __forceinline__ unsigned *trace_counters()
 __device__ __forceinline__ void trace_init()
 {
 #ifdef Q4MM_TRACE
-    if (threadIdx.x < 64) trace_counters()[threadIdx.x] = 0u;
+    if (threadIdx.x < kTraceRegions) trace_counters()[threadIdx.x] = 0u;
 #endif
 }
 
@@ -61,7 +64,7 @@ __device__ __forceinline__ void trace(const TraceRef &t, unsigned ev, unsigned a
 {
 #ifdef Q4MM_TRACE
     const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (t.buf && blockIdx.x == t.cta && lane < 4 && warp < 16) {
+    if (t.buf && blockIdx.x == t.cta && lane < 4 && warp < kTraceRegions / 4) {
         const unsigned region = warp * 4 + lane;
         const unsigned i = trace_counters()[region]++;
         if (i < t.cap) {
@@ -119,6 +122,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// The same test with cluster-scope acquire: for barriers that CTAs of the
+// cluster arrive on remotely, after writing this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Arrive, with cluster-scope release, on a barrier in another CTA of the
+// cluster (`cluster_addr` from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete, for at most
@@ -366,6 +401,13 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp receives
 // lane (base lane + i), columns col..col+15.
+__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t r[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t r[16])
 {
     asm volatile(
@@ -390,6 +432,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t r[32
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
+        : "memory");
+}
+
+// Thread i of the warp writes its 16 registers to lane (base lane + i),
+// columns col..col+15.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t r[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 

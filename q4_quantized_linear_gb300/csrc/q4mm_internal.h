@@ -41,7 +41,9 @@ struct DeviceInfo {
 // (device, kernel).
 cudaError_t set_max_smem(const void *func, size_t bytes);
 
-// Event-trace destination the kernels record into (profiling builds only).
+// Event-trace destination the kernels record into (profiling builds only):
+// one region of records per recording thread, lanes 0..3 of warps 0..23.
+constexpr unsigned kTraceRegions = 96;
 struct TraceSettings {
     unsigned long long *buf = nullptr;
     unsigned cap = 0, cta = 0;
@@ -72,8 +74,9 @@ struct DecodeArgs {
     int m, n, nb, np, groups;
     int pass_p0;           // first pair of this launch's K range
     int S, pbase, prem;    // K slices of the range: slice s has pbase + (s < prem) pairs
+    int clusters;          // clusters in the grid: cluster c owns groups c, c + clusters, ...
+    int ring;              // weight-record ring depth (>= 4)
     int accumulate;        // add into Y instead of overwriting it
-    int ring;              // weight-record ring depth
     int xs_bytes;          // shared bytes of the staged X image
     int prefetch_w;        // stream W before waiting on the preceding kernel
     unsigned long long *trace_buf;
@@ -85,8 +88,10 @@ struct DecodePlan {
     int S = 1;             // K slices = cluster size
     int passes = 1;        // launches over consecutive K ranges
     int pairs_per_pass = 0;
-    int ring = 8;
-    int ctas = 0;          // grid size per pass (tiles x S)
+    int clusters = 0;      // persistent clusters per launch
+    int ctas = 0;          // clusters x S
+    int ring = 8;          // weight-record ring depth (multiple of 4 and of sets)
+    int sets = 2;          // dequantiser sets (2 or 3)
     int xs_bytes = 0;
     size_t smem = 0;
 };

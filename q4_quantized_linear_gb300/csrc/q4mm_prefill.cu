@@ -20,7 +20,8 @@
 //                   alternating pairs); then the epilogue, TMEM -> Y
 //      tcgen05.mma kind::f16 (bf16, fp32 accumulate in TMEM), A = the
 //      dequantised weights read from tensor memory, B = the X tile in shared
-//      memory, M = 128 weight rows, N = T tokens (256 + rest when T > 256).
+//      memory, M = 128 weight rows, N = T tokens (two near-equal MMAs per
+//      K step when T > 256).
 //      The weight operand never touches shared memory, which leaves shared
 //      bandwidth to the X tiles. Every ring is an mbarrier pipeline; every
 //      wait is time-bounded.
@@ -42,6 +43,9 @@ constexpr int kProducerLanes = 4;
 
 __global__ void __launch_bounds__(256) xcast_kernel(const XcastArgs a)
 {
+    // The GEMM that follows may be scheduled at once: before its own
+    // dependency wait it only streams and dequantises weights.
+    pdl_launch_dependents();
     pdl_wait();
     const int64_t total = static_cast<int64_t>(a.ts) * a.np * a.T * 8;
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < total;
@@ -70,7 +74,6 @@ __global__ void __launch_bounds__(256) xcast_kernel(const XcastArgs a)
         uint8_t *dst = a.ximg + rowid * 128 + ((c ^ (r & 7)) << 4);
         *reinterpret_cast<uint4 *>(dst) = out;
     }
-    pdl_launch_dependents();
 }
 
 // -------------------------------------------------------------- gemm -----
@@ -90,10 +93,18 @@ __device__ __forceinline__ void fail(const Smem &sm, const PrefillArgs &a)
     record_status(a.status, kErrTimeout);
 }
 
+// Bounded wait by every lane of a warp with one outcome for the whole warp:
+// a timeout must not leave a warp diverged in front of .aligned tcgen05 code.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, limit_ns)) != 0;
+}
+
 // One row's pair of blocks -> 32 bf16x2 columns of tensor memory, in the
 // order the MMA's K runs: column 16 blk + 4 wd + j holds v[j] of nibble word
 // wd of block blk, i.e. block elements 4 wd + {0,2 | 16,18 | 1,3 | 17,19}.
-// Each weight is the exact (q - 8) times d rounded to bf16, rounded once.
+// Each weight is (q - 8), exact, times d rounded to bf16; the product is
+// rounded to bf16 once more.
 __device__ __forceinline__ void dequant_pair_bf16(uint32_t d01, uint4 q0, uint4 q1, uint32_t out[32])
 {
 #pragma unroll
@@ -183,11 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
         }
     }
 
-    pdl_wait();
-    if (tid == 0) trace(tr, kTrPdl, 0);
-
     if (warp == 0) {
         // ---------------------------------------------------------- producer
+        // Only the X tiles come from the preceding kernel (the X cast); the
+        // other warps touch shared and tensor memory only until the
+        // epilogue, which follows the last MMA and so this wait.
+        pdl_wait();
+        if (tid == 0) trace(tr, kTrPdl, 0);
         if (producer) {
             const uint64_t pol = policy_evict_last();
             int last_b = -1, last_w = -1;
@@ -209,38 +222,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
                 last_b = p;
             }
             if (last_w < 0 && w_issued_upto > lane) last_w = w_issued_upto - kProducerLanes;
-            // drain this lane's copies before the CTA may exit: the last copy
-            // into each slot it owns
-            for (int p = last_w; p >= 0 && p > last_w - R; p -= kProducerLanes)
+            // drain this lane's copies before the CTA may exit: only the last
+            // R pairs' copies can still be landing (a slot reused later has
+            // landed and been consumed)
+            for (int p = last_w; p >= 0 && p >= np - R; p -= kProducerLanes)
                 if (!mbar_wait(&sm.full_w[p % R], (p / R) & 1, a.wait_ns)) fail(sm, a);
-            for (int p = last_b; p >= 0 && p > last_b - R; p -= kProducerLanes)
+            for (int p = last_b; p >= 0 && p >= np - R; p -= kProducerLanes)
                 if (!mbar_wait(&sm.full_b[p % R], (p / R) & 1, a.wait_ns)) fail(sm, a);
         }
         __syncwarp();
     } else if (warp == 1) {
         // --------------------------------------------------------------- MMA
+        // One thread issues everything; descriptors are precomputed and the
+        // loop body is straight-line so MMAs issue back to back. Tiles wider
+        // than 256 tokens take two MMAs per K step of near-equal width (an
+        // N = 16 remainder would cost a full issue slot for little work).
         if (lane == 0) {
-            const int N1 = T > 256 ? 256 : T;
+            const int N1 = T > 256 ? ((T / 2 + 15) & ~15) : T;
             const int N2 = T - N1;
             const uint32_t id1 = idesc_bf16_f32(128, static_cast<uint32_t>(N1));
             const uint32_t id2 = idesc_bf16_f32(128, static_cast<uint32_t>(N2 > 0 ? N2 : 16));
-            const uint32_t b0 = smem_u32(sm.b);
-            for (int p = 0; p < np && !aborted(sm); ++p) {
-                const int sa = p % AST, sb = p % R;
-                if (!mbar_wait(&sm.full_a[sa], (p / AST) & 1, a.wait_ns)) { fail(sm, a); break; }
-                if (!mbar_wait(&sm.full_b[sb], (p / R) & 1, a.wait_ns)) { fail(sm, a); break; }
+            const uint32_t d2 = tmem + static_cast<uint32_t>(N1);
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sm.b));
+            const uint64_t bstep = static_cast<uint64_t>(bstage >> 4);
+            const uint64_t b2 = static_cast<uint64_t>((N1 * 128) >> 4);
+            uint64_t bd = bdesc0;
+            uint32_t at = tmem + acol0;
+            int sa = 0, sb = 0;
+            uint32_t pha = 0, phb = 0, acc = 0;
+            for (int p = 0; p < np; ++p) {
+                if (!mbar_wait(&sm.full_a[sa], pha, a.wait_ns)) { fail(sm, a); break; }
+                if (!mbar_wait(&sm.full_b[sb], phb, a.wait_ns)) { fail(sm, a); break; }
                 trace(tr, kTrMmaIssue, static_cast<unsigned>(p));
                 tc_fence_after();
-                const uint32_t at = tmem + acol0 + static_cast<uint32_t>(sa) * 32u;
-                const uint32_t bs = b0 + static_cast<uint32_t>(sb) * bstage;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t acc = (p | kk) != 0;
-                    tc_mma_f16_ts(tmem, at + 8 * kk, smem_desc_sw128(bs + kk * 32), id1, acc);
-                    if (N2 > 0) tc_mma_f16_ts(tmem + 256, at + 8 * kk, smem_desc_sw128(bs + 256 * 128 + kk * 32), id2, acc);
+                if (N2 > 0) {
+                    tc_mma_f16_ts(tmem, at, bd, id1, acc);
+                    tc_mma_f16_ts(d2, at, bd + b2, id2, acc);
+                    tc_mma_f16_ts(tmem, at + 8u, bd + 2u, id1, 1u);
+                    tc_mma_f16_ts(d2, at + 8u, bd + b2 + 2u, id2, 1u);
+                    tc_mma_f16_ts(tmem, at + 16u, bd + 4u, id1, 1u);
+                    tc_mma_f16_ts(d2, at + 16u, bd + b2 + 4u, id2, 1u);
+                    tc_mma_f16_ts(tmem, at + 24u, bd + 6u, id1, 1u);
+                    tc_mma_f16_ts(d2, at + 24u, bd + b2 + 6u, id2, 1u);
+                } else {
+                    tc_mma_f16_ts(tmem, at, bd, id1, acc);
+                    tc_mma_f16_ts(tmem, at + 8u, bd + 2u, id1, 1u);
+                    tc_mma_f16_ts(tmem, at + 16u, bd + 4u, id1, 1u);
+                    tc_mma_f16_ts(tmem, at + 24u, bd + 6u, id1, 1u);
                 }
                 tc_commit(&sm.empty_a[sa]);
                 tc_commit(&sm.empty_b[sb]);
+                acc = 1u;
+                if (++sa == AST) { sa = 0; pha ^= 1u; at = tmem + acol0; } else { at += 32u; }
+                if (++sb == R) { sb = 0; phb ^= 1u; bd = bdesc0; } else { bd += bstep; }
             }
             tc_commit(sm.done); // also taken on abort: no MMA of ours is in flight past this
         }
@@ -252,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
         const int h = dw >> 2;             // which pairs: p % 2 == h
         const int row = q * 32 + lane;     // weight row within the tile
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        for (int p = h; p < np && !aborted(sm); p += 2) {
+        for (int p = h; p < np && !__any_sync(0xFFFFFFFFu, aborted(sm)); p += 2) {
             const int sw = p % R, sa = p % AST;
-            if (!mbar_wait(&sm.full_w[sw], (p / R) & 1, a.wait_ns)) { fail(sm, a); break; }
+            if (!warp_wait(&sm.full_w[sw], (p / R) & 1, a.wait_ns)) { fail(sm, a); break; }
             if (lane == 0) trace(tr, kTrWFull, static_cast<unsigned>(p));
-            if (!mbar_wait(&sm.empty_a[sa], ((p / AST) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
+            if (!warp_wait(&sm.empty_a[sa], ((p / AST) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
             const uint8_t *rec = sm.w + static_cast<size_t>(sw) * kRecordBytes;
             const uint32_t d01 = *reinterpret_cast<const uint32_t *>(rec + kRecScaleOff + 4 * row);
             const uint4 q0 = lds128(rec + kRecQs0Off + 16 * row);
@@ -276,13 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
 
         // epilogue: this warp's TMEM sub-partition, half of the token columns
         const int64_t grow = static_cast<int64_t>(rt) * 128 + row;
-        if (!mbar_wait(sm.done, 0, a.wait_ns)) fail(sm, a);
+        const bool done_ok = warp_wait(sm.done, 0, a.wait_ns);
+        if (!done_ok) fail(sm, a);
         if (lane == 0) trace(tr, kTrDone, 0);
         tc_fence_after();
         pdl_launch_dependents();
         const int chunks = T / 16;
         const int c_lo = h * ((chunks + 1) / 2), c_hi = h ? chunks : (chunks + 1) / 2;
-        for (int cc = c_lo; cc < c_hi; ++cc) {
+        for (int cc = c_lo; done_ok && cc < c_hi; ++cc) {
             const int c0 = cc * 16;
             uint32_t r[16];
             tmem_ld_32x32b_x16(tmem + lane_base + static_cast<uint32_t>(c0), r);
@@ -355,12 +390,16 @@ bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *pl
     if (best.T == 0) return false;
     best.rowtiles = static_cast<int>(rowtiles);
     const int acol0 = (best.T + 31) & ~31;
-    best.astages = std::min(8, (512 - acol0) / 32);
+    // even, so that each stage always belongs to one of the two dequantiser
+    // sets (parity waits need a single waiter per barrier)
+    best.astages = std::min(8, (512 - acol0) / 32) & ~1;
     if (best.astages < 2) return false;
     best.ring = 8;
     if (gemm_smem_bytes(best.T, best.ring, best.astages) > kSmemOptIn) best.ring = 4;
     best.smem = gemm_smem_bytes(best.T, best.ring, best.astages);
     if (best.smem > kSmemOptIn) return false;
+    // one CTA per SM: each holds all 512 tensor-memory columns
+    best.smem = std::max<size_t>(best.smem, kSmemPerSM / 2 + 1024);
     best.ws_ximg_off = kWsReservedBytes;
     best.ws_bytes = kWsReservedBytes + static_cast<size_t>(best.ts) * np * best.T * 128;
     *plan = best;
