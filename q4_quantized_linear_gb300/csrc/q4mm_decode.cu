@@ -596,7 +596,8 @@ size_t decode_smem(int N, int P, int S, int64_t m, int ring)
 // Cost, in record times of one SM's share of HBM: the busiest SM's records,
 // or one CTA's records at the rate a single CTA's ring sustains (kCtaRate of
 // the share at a ring of 8, in proportion to the ring), whichever is larger,
-// plus per-group and per-CTA overheads.
+// plus per-group and per-CTA overheads, plus the start-up time that cannot
+// overlap the preceding call when every SM already holds two CTAs.
 bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan)
 {
     if (m < 1 || m > 16 || sm_count < 1) return false;
@@ -633,8 +634,11 @@ bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan
             const double sm_pairs = (ctas > sm_count ? 2.0 : 1.0) * cta_pairs;
             const double rate = std::min(1.0, kCtaRate * ring / 8.0);
             const double stream = std::max({sm_pairs, cta_pairs / rate, static_cast<double>(groups * ppp) / sm_count});
+            // A grid of more than one CTA per SM leaves no room for the next
+            // call's CTAs to start streaming while this one finishes.
+            const double no_overlap = ctas > sm_count ? 12.0 : 0.0;
             const double cost = static_cast<double>(passes) *
-                                (stream + static_cast<double>(tiles_per) * (1.5 + (S > 1 ? 1.0 : 0.0)) + 6.0);
+                                (stream + static_cast<double>(tiles_per) * (1.5 + (S > 1 ? 1.0 : 0.0)) + 6.0 + no_overlap);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.N = N;

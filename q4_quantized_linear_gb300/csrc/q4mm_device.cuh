@@ -139,15 +139,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
-{
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
 
 // Arrive, with cluster-scope release, on a barrier in another CTA of the
 // cluster (`cluster_addr` from mapa_shared).
@@ -156,6 +147,36 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// The same tests, letting the hardware suspend the thread for up to
+// `hint_ns` until the phase completes (a waiting warp then issues nothing).
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster_for(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspension granted per try while waiting (the bound is checked between tries).
+constexpr uint32_t kSuspendHintNs = 100000;
+
 // Wait for the phase of `bar` with parity `parity` to complete, for at most
 // limit_ns nanoseconds. Returns false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
@@ -163,7 +184,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_for(bar, parity, kSuspendHintNs)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster_for(bar, parity, kSuspendHintNs)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -401,6 +432,20 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp receives
 // lane (base lane + i), columns col..col+15.
+__device__ __forceinline__ void tmem_ld_32x32b_x2(uint32_t taddr, uint32_t r[2])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t r[4])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+// Width-generic load of W consecutive columns (W in 2, 4, 8, 16, 32).
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t *r);
 __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t r[8])
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -434,6 +479,11 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t r[32
         : "r"(taddr)
         : "memory");
 }
+template <> __device__ __forceinline__ void tmem_ld_cols<2>(uint32_t t, uint32_t *r) { tmem_ld_32x32b_x2(t, r); }
+template <> __device__ __forceinline__ void tmem_ld_cols<4>(uint32_t t, uint32_t *r) { tmem_ld_32x32b_x4(t, r); }
+template <> __device__ __forceinline__ void tmem_ld_cols<8>(uint32_t t, uint32_t *r) { tmem_ld_32x32b_x8(t, r); }
+template <> __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t t, uint32_t *r) { tmem_ld_32x32b_x16(t, r); }
+template <> __device__ __forceinline__ void tmem_ld_cols<32>(uint32_t t, uint32_t *r) { tmem_ld_32x32b_x32(t, r); }
 
 // Thread i of the warp writes its 16 registers to lane (base lane + i),
 // columns col..col+15.
