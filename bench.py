@@ -415,7 +415,7 @@ def native(args):
         },
         "roofline": {
             "bound": "tensor" if tensor else "hbm",
-            "kernel": "gemm_kernel (after xcast_kernel)" if tensor else f"decode_kernel<{1 if m <= 8 else 2}>",
+            "kernel": "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)" if tensor else "decode_kernel (q4mm_decode.cu)",
             "achieved": achieved,
             "peak": peak,
             "unit": unit,
