@@ -196,9 +196,28 @@ class Workload:
                              self.ws, self.wsb, stream)
 
 
-def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None):
-    """Run `warmup` then time exactly `steps` steps as CUDA-graph replays.
-    Returns elapsed seconds of the timed steps."""
+def reduce_max(value):
+    """Max of a float over the ranks of the default process group (NCCL on
+    the GPU, gloo on the host); the value itself without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, steps, units_per_step, slowest_sec):
+    """Units all ranks processed, divided by the slowest rank's time."""
+    return world * steps * units_per_step / slowest_sec
+
+
+def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None, barrier=None):
+    """Run `warmup` then time exactly `steps` steps as CUDA-graph replays,
+    bracketed by `barrier` (all ranks) and a device synchronize on both
+    sides. Returns elapsed seconds of the timed steps."""
     import torch
     per_graph = max(1, min(per_graph, steps))
     per_graph -= per_graph % wl.copies if per_graph >= wl.copies else 0
@@ -229,6 +248,9 @@ def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None):
         sampler.start()
         time.sleep(0.3)
     torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps // per_graph):
@@ -237,6 +259,8 @@ def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None):
             g_rest.replay()
         end.record(stream)
     torch.cuda.synchronize()
+    if barrier:
+        barrier()
     clocks = sampler.stop() if sampler else None
     return start.elapsed_time(end) / 1e3, clocks
 
@@ -352,26 +376,20 @@ def native(args):
     wl = Workload(q4lib, m, n, k)
 
     sampler = ClockSampler(local) if rank == 0 else None
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    sec, clocks = time_graph(q4lib, wl, args.steps, args.warmup, stream, sampler=sampler)
-    if world > 1:
-        t = torch.tensor([sec], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    barrier = dist.barrier if world > 1 else None
+    sec, clocks = time_graph(q4lib, wl, args.steps, args.warmup, stream, sampler=sampler, barrier=barrier)
+    sec = reduce_max(sec)
     unit = "TFLOP/s" if tensor else "GB/s"
     per_step_units = flops / 1e12 if tensor else wb / 1e9
-    value = world * args.steps * per_step_units / sec
+    value = whole_job_rate(world, args.steps, per_step_units, sec)
     per_launch = sec / args.steps
 
     e2e_steps = min(args.steps, 5000)
+    if barrier:
+        barrier()
     esec, h2d, d2h = time_e2e(q4lib, wl, e2e_steps, stream)
-    if world > 1:
-        t = torch.tensor([esec], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        esec = float(t.item())
-    e2e_value = world * e2e_steps * per_step_units / esec
+    esec = reduce_max(esec)
+    e2e_value = whole_job_rate(world, e2e_steps, per_step_units, esec)
 
     gpu_Y = wl.Yd.cpu().numpy()
     sweep = run_sweep(q4lib, stream, peaks) if (rank == 0 and not args.no_sweep) else None
@@ -440,6 +458,14 @@ def native(args):
         dist.destroy_process_group()
 
 
+def reference_sample_rows(n, steps, warmup, t_2048, budget_s=120.0):
+    """Rows of W per reference step so that warmup + steps oracle calls take
+    about budget_s, given t_2048 seconds for a 2048-row call (64-row units,
+    at least 64, at most 2048 and n)."""
+    rows = int(2048 * budget_s / max((steps + warmup) * t_2048, 1e-9))
+    return max(min(64, n), min(n, 2048, rows // 64 * 64))
+
+
 def reference(args):
     """The oracle (CPU, as it stands) on the same config and metric."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -454,8 +480,13 @@ def reference(args):
     wb = weight_bytes(n, k)
     blocks = synth.q4_0_blocks(n, k, seed=0)
     X = synth.activations(m, k, seed=0)
-    # each step is a bounded sample: a slice of rows sized so the run stays short
-    rows = min(n, 2048)
+    # Each step is a bounded sample: the leading rows of W, as many as keep
+    # the whole --warmup + --steps run near two minutes (calibrated on 2048).
+    oracle.matmul(blocks[:2048], X, 2048, k)
+    t0 = time.perf_counter()
+    oracle.matmul(blocks[:2048], X, 2048, k)
+    t_full = time.perf_counter() - t0
+    rows = reference_sample_rows(n, args.steps, args.warmup, t_full)
     sample_bytes = weight_bytes(rows, k)
     for _ in range(args.warmup):
         oracle.matmul(blocks[:rows], X, rows, k)
