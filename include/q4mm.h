@@ -145,6 +145,28 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
                             int64_t m, int64_t k, int64_t n,
                             void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
 
+/* Size of the library's fixed scratch array used by q4_0_matmul_static_scratch. */
+#define Q4_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* As q4_0_matmul, but with no allocation of any kind: the scratch is a fixed
+ * array of Q4_STATIC_SCRATCH_BYTES (8 MiB) in the library's device memory,
+ * one per device. The pages have no counterpart; this form exists for
+ * callers that must not allocate device memory. Only m > 16 uses scratch.
+ *   Limit: shapes with q4_0_matmul_workspace_size(m, k, n) above
+ *   Q4_STATIC_SCRATCH_BYTES are refused with Q4_ERR_WORKSPACE before anything
+ *   is launched (m = 540, n = 9728, k = 2560 needs about 3 MiB).
+ *   Set-up: the first call on a device, with that device current, looks up
+ *   the array's address (cudaGetSymbolAddress, return code checked) and
+ *   zeroes its reserved head with a synchronous cudaMemset. Make that first
+ *   call before any stream capture; later calls only enqueue work on
+ *   `stream`.
+ *   Races: every call on a device shares the one array, so calls that can
+ *   overlap (other streams, other threads) race; calls in one stream are
+ *   ordered.
+ * Arguments, precision and status codes as q4_0_matmul. */
+Q4MM_API int q4_0_matmul_static_scratch(const void *W_packed, const float *X, float *Y,
+                                        int64_t m, int64_t k, int64_t n, q4mm_stream_t stream);
+
 /* Continuous batching: m active slots share one read of the weights.
  * For i < m, row slot_ids[i] of X_slots produces row slot_ids[i] of Y_slots;
  * every other row of Y_slots is left untouched. Equivalent to gathering the

@@ -38,6 +38,7 @@ _SIGS = {
     "q4_0_matmul_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "q4_0_matmul": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_ws": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "q4_0_matmul_static_scratch": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots_ws": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "q4_status_string": (ctypes.c_char_p, [_INT]),
@@ -134,6 +135,14 @@ def q4_0_matmul_ws(W_packed, X, Y, m: int, k: int, n: int, workspace, workspace_
     rc = _lib.q4_0_matmul_ws(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _addr(workspace),
                              workspace_bytes, _stream(stream))
     return _check(rc, "q4_0_matmul_ws") if check else rc
+
+
+Q4_STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def q4_0_matmul_static_scratch(W_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_matmul_static_scratch(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _stream(stream))
+    return _check(rc, "q4_0_matmul_static_scratch") if check else rc
 
 
 def q4_0_matmul_batched_slots(W_packed, X_slots, ldx: int, slot_ids, m: int, Y_slots, ldy: int,
