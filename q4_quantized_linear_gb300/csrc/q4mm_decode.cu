@@ -626,31 +626,36 @@ bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan
             }
             if (ring == 0) continue;                          // more passes: smaller slices
             const size_t smem = std::max(decode_smem(N, static_cast<int>(P), S, m, ring), smem_min);
-            const int64_t clusters = std::min<int64_t>(groups, (2 * sm_count) / S);
-            if (clusters < 1) break;
-            const int64_t tiles_per = ceil_div(groups, clusters);
-            const int64_t ctas = clusters * S;
-            const double cta_pairs = static_cast<double>(tiles_per * P);
-            const double sm_pairs = (ctas > sm_count ? 2.0 : 1.0) * cta_pairs;
-            const double rate = std::min(1.0, kCtaRate * ring / 8.0);
-            const double stream = std::max({sm_pairs, cta_pairs / rate, static_cast<double>(groups * ppp) / sm_count});
-            // A grid of more than one CTA per SM leaves no room for the next
-            // call's CTAs to start streaming while this one finishes.
-            const double no_overlap = ctas > sm_count ? 12.0 : 0.0;
-            const double cost = static_cast<double>(passes) *
-                                (stream + static_cast<double>(tiles_per) * (1.5 + (S > 1 ? 1.0 : 0.0)) + 6.0 + no_overlap);
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
-                best.N = N;
-                best.S = S;
-                best.passes = static_cast<int>(passes);
-                best.pairs_per_pass = static_cast<int>(ppp);
-                best.clusters = static_cast<int>(clusters);
-                best.ctas = static_cast<int>(ctas);
-                best.ring = ring;
-                best.sets = sets;
-                best.xs_bytes = static_cast<int>(round_up(P * N * 128, 1024));
-                best.smem = smem;
+            // one CTA per SM (room for the next call to overlap) or two
+            for (int per = 1; per <= 2; ++per) {
+                const int64_t clusters = std::min<int64_t>(groups, (per * sm_count) / S);
+                if (clusters < 1) continue;
+                const int64_t tiles_per = ceil_div(groups, clusters);
+                const int64_t ctas = clusters * S;
+                const double cta_pairs = static_cast<double>(tiles_per * P);
+                const double sm_pairs = (ctas > sm_count ? 2.0 : 1.0) * cta_pairs;
+                const double rate = std::min(1.0, kCtaRate * ring / 8.0);
+                const double stream =
+                    std::max({sm_pairs, cta_pairs / rate, static_cast<double>(groups * ppp) / sm_count});
+                // A grid of more than one CTA per SM leaves no room for the next
+                // call's CTAs to start streaming while this one finishes.
+                const double no_overlap = ctas > sm_count ? 12.0 : 0.0;
+                const double cost = static_cast<double>(passes) *
+                                    (stream + static_cast<double>(tiles_per) * (1.5 + (S > 1 ? 1.0 : 0.0)) + 6.0 +
+                                     no_overlap);
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    best.N = N;
+                    best.S = S;
+                    best.passes = static_cast<int>(passes);
+                    best.pairs_per_pass = static_cast<int>(ppp);
+                    best.clusters = static_cast<int>(clusters);
+                    best.ctas = static_cast<int>(ctas);
+                    best.ring = ring;
+                    best.sets = sets;
+                    best.xs_bytes = static_cast<int>(round_up(P * N * 128, 1024));
+                    best.smem = smem;
+                }
             }
             break;                                            // fewest passes that fit
         }
