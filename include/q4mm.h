@@ -204,14 +204,13 @@ Q4MM_API int q4_last_device_status(int clear);
 Q4MM_API int q4_set_wait_limit_ns(uint64_t ns);
 
 /* Declare packed weights read-only while matmuls run (default: not declared).
- * When enabled, a decode-path kernel (m <= 16) starts streaming W_packed
- * before the kernel that precedes it in the stream has finished, overlapping
- * the two (programmatic dependent launch); X, Y and the workspace are still
- * read only after that kernel completes. Enable it only if no kernel writes a
- * W_packed immediately before a matmul that reads it in the same stream
- * (after q4_0_pack, synchronise or record an event before the first matmul).
- * The prefill path always overlaps its weight reads: the kernel before its
- * GEMM is its own X cast. Applies to launches made after the call. */
+ * When enabled, the matmul kernels (the decode kernel, and the prefill GEMM)
+ * start streaming W_packed before the kernels that precede them in the
+ * stream have finished, overlapping the two (programmatic dependent launch);
+ * X, Y and the workspace are still read only after those kernels complete.
+ * Enable it only if no kernel writes a W_packed immediately before a matmul
+ * that reads it in the same stream (after q4_0_pack, synchronise or record an
+ * event before the first matmul). Applies to launches made after the call. */
 Q4MM_API int q4_set_weight_prefetch(int enable);
 
 /* Profiling builds only (compiled with -DQ4MM_TRACE): kernels launched after

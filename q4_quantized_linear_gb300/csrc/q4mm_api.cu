@@ -211,8 +211,10 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     pa.groups = static_cast<int>(ceil_div(n, kGroupRows));
     pa.T = plan.T;
     pa.ts = plan.ts;
-    pa.ring = plan.ring;
+    pa.bring = plan.bring;
+    pa.wring = plan.wring;
     pa.astages = plan.astages;
+    pa.prefetch_w = g_prefetch_w.load();
     return map_cuda(launch_prefill(plan, xa, pa, s));
 }
 

@@ -41,7 +41,7 @@ struct TraceRef {
 enum TraceEvent : unsigned {
     kTrStart = 1, kTrPdl = 2, kTrXStaged = 3, kTrWIssue = 4, kTrWFull = 5, kTrDeqDone = 6,
     kTrMmaIssue = 7, kTrBIssue = 8, kTrDone = 9, kTrEpiDone = 10, kTrEnd = 11, kTrBFull = 12,
-    kTrSetup = 13, kTrTile = 14, kTrAlloc = 15, kTrXLoaded = 16, kTrXScaled = 17, kTrRed = 18
+    kTrSetup = 13, kTrTile = 14, kTrAlloc = 15, kTrXLoaded = 16, kTrXScaled = 17, kTrRed = 18, kTrAFull = 19
 };
 
 #ifdef Q4MM_TRACE
@@ -221,6 +221,13 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
         "%4;" ::"r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Asynchronous prefetch of `bytes` at `src` into L2 (no completion signal).
+// src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first()

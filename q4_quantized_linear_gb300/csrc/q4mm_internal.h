@@ -111,8 +111,10 @@ struct PrefillArgs {
     uint64_t wait_ns;
     int m, n, np, groups;
     int T, ts;              // tokens per tile, token tiles
-    int ring;               // X-tile and weight-record ring depth
+    int bring;              // X-tile ring depth
+    int wring;              // weight-record ring depth (even: two dequantiser sets)
     int astages;            // dequantised weight stages in tensor memory
+    int prefetch_w;         // stream W before waiting on the preceding kernel
     unsigned long long *trace_buf;
     unsigned trace_cap, trace_cta;
 };
@@ -128,7 +130,7 @@ struct XcastArgs {
 struct PrefillPlan {
     int T = 0, ts = 0;
     int rowtiles = 0;
-    int ring = 0, astages = 0;
+    int bring = 0, wring = 0, astages = 0;
     size_t smem = 0;
     size_t ws_bytes = 0;    // reserved region + X image bytes
     size_t ws_ximg_off = 0;

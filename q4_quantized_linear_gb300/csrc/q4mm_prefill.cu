@@ -11,17 +11,26 @@
 //      elements follow the order the weight dequantiser emits), so the GEMM
 //      fetches each X tile with one 1-D bulk copy.
 //   2. gemm: one CTA per (128 weight rows) x (T tokens). Warp roles:
-//        warp 0     producer: lanes 0..3 each own every fourth pair and issue
-//                   its packed weight record and X tile copies
-//        warp 1     tensor-memory allocation and the single MMA thread
+//        warp 0     X-tile producer (one lane), ring as deep as shared
+//                   memory allows: its copies take over a microsecond to land
+//        warp 1     tensor-memory allocation; MMA thread for the first half
+//                   of the token columns (all of them when T = 16)
 //        warps 2-9  dequantise: each thread owns one weight row and writes
 //                   the pair's 64 bf16 weights, (q - 8) times d, straight
 //                   into tensor memory (two warps per TMEM sub-partition,
 //                   alternating pairs); then the epilogue, TMEM -> Y
+//        warp 10    weight-record producer (one lane), its own ring. The two
+//                   producers sit in different warps: a lane asleep in a
+//                   suspend-hinted barrier wait holds up its whole warp.
+//        warp 11    MMA thread for the other half of the token columns.
+//                   A thread gets only a few hundred cycles of MMA work
+//                   ahead of the tensor pipe before its issue blocks, so each
+//                   thread's waits and commits between pairs would leave the
+//                   pipe idle; with two issuers one fills the other's gaps.
 //      tcgen05.mma kind::f16 (bf16, fp32 accumulate in TMEM), A = the
 //      dequantised weights read from tensor memory, B = the X tile in shared
 //      memory, M = 128 weight rows, N = T tokens (two near-equal MMAs per
-//      K step when T > 256).
+//      K step, one from each MMA thread, when T >= 32).
 //      The weight operand never touches shared memory, which leaves shared
 //      bandwidth to the X tiles. Every ring is an mbarrier pipeline; every
 //      wait is time-bounded.
@@ -36,8 +45,10 @@ namespace {
 
 constexpr int kErrTimeout = 5;
 constexpr int kDequantWarps = 8;
-constexpr int kThreads = (2 + kDequantWarps) * 32;
-constexpr int kProducerLanes = 4;
+constexpr int kWProducerWarp = 2 + kDequantWarps;
+constexpr int kMma2Warp = 3 + kDequantWarps;
+constexpr int kWPrefetch = 8; // weight records requested into L2 beyond the ring
+constexpr int kThreads = (4 + kDequantWarps) * 32;
 
 // ------------------------------------------------------------- xcast -----
 
@@ -134,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
     const int jt = blockIdx.x % a.ts; // token tile
     const int T = a.T;
     const int np = a.np;
-    const int R = a.ring;
+    const int RB = a.bring, RW = a.wring;
     const int AST = a.astages;
     const uint32_t bstage = static_cast<uint32_t>(T) * 128u;
     const uint32_t acol0 = static_cast<uint32_t>((T + 31) & ~31); // first A column after D
@@ -144,25 +155,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
 
     Smem sm;
     sm.b = base;
-    sm.w = sm.b + static_cast<size_t>(R) * bstage;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.w + static_cast<size_t>(R) * kRecordBytes);
+    sm.w = sm.b + static_cast<size_t>(RB) * bstage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm.w + static_cast<size_t>(RW) * kRecordBytes);
     sm.full_b = bars;
-    sm.empty_b = sm.full_b + R;
-    sm.full_w = sm.empty_b + R;
-    sm.empty_w = sm.full_w + R;
-    sm.full_a = sm.empty_w + R;
+    sm.empty_b = sm.full_b + RB;
+    sm.full_w = sm.empty_b + RB;
+    sm.empty_w = sm.full_w + RW;
+    sm.full_a = sm.empty_w + RW;
     sm.empty_a = sm.full_a + AST;
     sm.done = sm.empty_a + AST;
     sm.tmem_slot = reinterpret_cast<uint32_t *>(sm.done + 1);
     sm.abort = reinterpret_cast<int *>(sm.tmem_slot + 1);
 
+    // Token columns [0, N1) go to the MMA thread of warp 1, [N1, T) to the
+    // one of warp 11, in near-equal halves (each a multiple of 16) whenever
+    // the tile has two; a 16-token tile has one MMA thread.
+    const int N1 = T >= 32 ? ((T / 2 + 15) & ~15) : T;
+    const int N2 = T - N1;
+    const uint32_t issuers = N2 > 0 ? 2u : 1u;
     if (tid == 0) {
-        for (int i = 0; i < R; ++i) {
-            mbar_init(&sm.full_b[i], 1), mbar_init(&sm.empty_b[i], 1);
-            mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], kDequantWarps / 2);
-        }
-        for (int i = 0; i < AST; ++i) mbar_init(&sm.full_a[i], kDequantWarps / 2), mbar_init(&sm.empty_a[i], 1);
-        mbar_init(sm.done, 1);
+        for (int i = 0; i < RB; ++i) mbar_init(&sm.full_b[i], 1), mbar_init(&sm.empty_b[i], issuers);
+        for (int i = 0; i < RW; ++i) mbar_init(&sm.full_w[i], 1), mbar_init(&sm.empty_w[i], kDequantWarps / 2);
+        for (int i = 0; i < AST; ++i) mbar_init(&sm.full_a[i], kDequantWarps / 2), mbar_init(&sm.empty_a[i], issuers);
+        mbar_init(sm.done, issuers);
         *sm.abort = 0;
         fence_barrier_init();
     }
@@ -177,104 +192,97 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
 
     const uint8_t *wsrc = a.W + static_cast<int64_t>(rt) * np * kRecordBytes;
     const uint8_t *xsrc = a.ximg + static_cast<size_t>(jt) * np * bstage;
-    const bool producer = warp == 0 && lane < kProducerLanes;
-    int w_issued_upto = lane; // producer lane: next pair whose weight record it issues
-
-    // The packed weights never come from the preceding kernel (that is always
-    // this call's X cast), so each producer lane requests its first weight
-    // records before the dependency wait.
-    if (producer) {
-        const uint64_t pol = policy_evict_last();
-        for (; w_issued_upto < np && w_issued_upto < R; w_issued_upto += kProducerLanes) {
-            const int p = w_issued_upto;
-            trace(tr, kTrWIssue, static_cast<unsigned>(p));
-            mbar_arrive_expect_tx(&sm.full_w[p % R], kRecordBytes);
-            bulk_g2s_hint(sm.w + static_cast<size_t>(p % R) * kRecordBytes, wsrc + static_cast<size_t>(p) * kRecordBytes,
-                          kRecordBytes, &sm.full_w[p % R], pol);
-        }
-    }
+    // One lane streams the X tiles, another (in another warp) the weight
+    // records, each in pair order through its own ring (one owner per slot).
+    const uint64_t pol = policy_evict_last();
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
+        // ---------------------------------------------------- X-tile producer
         // Only the X tiles come from the preceding kernel (the X cast); the
-        // other warps touch shared and tensor memory only until the
+        // dequantisers touch shared and tensor memory only until the
         // epilogue, which follows the last MMA and so this wait.
         pdl_wait();
         if (tid == 0) trace(tr, kTrPdl, 0);
-        if (producer) {
-            const uint64_t pol = policy_evict_last();
-            int last_b = -1, last_w = -1;
-            for (int p = lane; p < np && !aborted(sm); p += kProducerLanes) {
-                const int s = p % R;
-                if (p >= w_issued_upto) {
-                    if (!mbar_wait(&sm.empty_w[s], ((p / R) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
-                    trace(tr, kTrWIssue, static_cast<unsigned>(p));
-                    mbar_arrive_expect_tx(&sm.full_w[s], kRecordBytes);
-                    bulk_g2s_hint(sm.w + static_cast<size_t>(s) * kRecordBytes, wsrc + static_cast<size_t>(p) * kRecordBytes,
-                                  kRecordBytes, &sm.full_w[s], pol);
-                }
-                last_w = p;
-                if (!mbar_wait(&sm.empty_b[s], ((p / R) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
+        if (lane == 0) {
+            int s = 0, last = -1;
+            uint32_t ph = 0;
+            for (int p = 0; p < np && !aborted(sm); ++p) {
+                if (p >= RB && !mbar_wait(&sm.empty_b[s], ph ^ 1u, a.wait_ns)) { fail(sm, a); break; }
                 trace(tr, kTrBIssue, static_cast<unsigned>(p));
                 mbar_arrive_expect_tx(&sm.full_b[s], bstage);
                 bulk_g2s_hint(sm.b + static_cast<size_t>(s) * bstage, xsrc + static_cast<size_t>(p) * bstage, bstage,
                               &sm.full_b[s], pol);
-                last_b = p;
+                last = p;
+                if (++s == RB) s = 0, ph ^= 1u;
             }
-            if (last_w < 0 && w_issued_upto > lane) last_w = w_issued_upto - kProducerLanes;
-            // drain this lane's copies before the CTA may exit: only the last
-            // R pairs' copies can still be landing (a slot reused later has
-            // landed and been consumed)
-            for (int p = last_w; p >= 0 && p >= np - R; p -= kProducerLanes)
-                if (!mbar_wait(&sm.full_w[p % R], (p / R) & 1, a.wait_ns)) fail(sm, a);
-            for (int p = last_b; p >= 0 && p >= np - R; p -= kProducerLanes)
-                if (!mbar_wait(&sm.full_b[p % R], (p / R) & 1, a.wait_ns)) fail(sm, a);
+            // no copy may still be landing when the CTA exits: only the last
+            // RB tiles' copies can be (a slot reused later has landed)
+            for (int p = last; p >= 0 && p >= np - RB; --p)
+                if (!mbar_wait(&sm.full_b[p % RB], (p / RB) & 1, a.wait_ns)) fail(sm, a);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // --------------------------------------------------------------- MMA
-        // One thread issues everything; descriptors are precomputed and the
-        // loop body is straight-line so MMAs issue back to back. Tiles wider
-        // than 256 tokens take two MMAs per K step of near-equal width (an
-        // N = 16 remainder would cost a full issue slot for little work).
+    } else if (warp == kWProducerWarp) {
+        // ---------------------------------------------- weight-record producer
+        // With the weights declared read-only the records stream before the
+        // dependency wait (no kernel in flight writes them); otherwise the
+        // preceding kernels must have finished first.
+        // The ring is shallow (shared memory goes to the X tiles), so records
+        // further ahead are pulled into L2 first: a slot then waits out an L2
+        // hit, not an HBM round trip.
+        if (!a.prefetch_w) pdl_wait();
         if (lane == 0) {
-            const int N1 = T > 256 ? ((T / 2 + 15) & ~15) : T;
-            const int N2 = T - N1;
-            const uint32_t id1 = idesc_bf16_f32(128, static_cast<uint32_t>(N1));
-            const uint32_t id2 = idesc_bf16_f32(128, static_cast<uint32_t>(N2 > 0 ? N2 : 16));
-            const uint32_t d2 = tmem + static_cast<uint32_t>(N1);
-            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sm.b));
+            int s = 0, last = -1;
+            uint32_t ph = 0;
+            for (int p = RW; p < np && p < RW + kWPrefetch; ++p)
+                bulk_prefetch_l2(wsrc + static_cast<size_t>(p) * kRecordBytes, kRecordBytes);
+            for (int p = 0; p < np && !aborted(sm); ++p) {
+                if (p >= RW && !mbar_wait(&sm.empty_w[s], ph ^ 1u, a.wait_ns)) { fail(sm, a); break; }
+                trace(tr, kTrWIssue, static_cast<unsigned>(p));
+                mbar_arrive_expect_tx(&sm.full_w[s], kRecordBytes);
+                bulk_g2s_hint(sm.w + static_cast<size_t>(s) * kRecordBytes, wsrc + static_cast<size_t>(p) * kRecordBytes,
+                              kRecordBytes, &sm.full_w[s], pol);
+                if (p + RW + kWPrefetch < np)
+                    bulk_prefetch_l2(wsrc + static_cast<size_t>(p + RW + kWPrefetch) * kRecordBytes, kRecordBytes);
+                last = p;
+                if (++s == RW) s = 0, ph ^= 1u;
+            }
+            for (int p = last; p >= 0 && p >= np - RW; --p)
+                if (!mbar_wait(&sm.full_w[p % RW], (p / RW) & 1, a.wait_ns)) fail(sm, a);
+        }
+        __syncwarp();
+    } else if (warp == 1 || warp == kMma2Warp) {
+        // --------------------------------------------------------------- MMA
+        // One thread per token-column range; descriptors are precomputed and
+        // the loop body is straight-line so its MMAs issue back to back. Both
+        // threads wait for every A stage and X tile and both commit to its
+        // release barrier (arrival count 2), so a slot is refilled only after
+        // both have finished with it: neither can fall a phase behind.
+        const bool second = warp == kMma2Warp;
+        if (lane == 0 && (!second || N2 > 0)) {
+            const uint32_t ncols = static_cast<uint32_t>(second ? N2 : N1);
+            const uint32_t idesc = idesc_bf16_f32(128, ncols);
+            const uint32_t d = tmem + (second ? static_cast<uint32_t>(N1) : 0u);
+            const uint64_t bdesc0 = smem_desc_sw128(smem_u32(sm.b)) + (second ? static_cast<uint64_t>((N1 * 128) >> 4) : 0u);
             const uint64_t bstep = static_cast<uint64_t>(bstage >> 4);
-            const uint64_t b2 = static_cast<uint64_t>((N1 * 128) >> 4);
             uint64_t bd = bdesc0;
             uint32_t at = tmem + acol0;
             int sa = 0, sb = 0;
             uint32_t pha = 0, phb = 0, acc = 0;
             for (int p = 0; p < np; ++p) {
                 if (!mbar_wait(&sm.full_a[sa], pha, a.wait_ns)) { fail(sm, a); break; }
+                trace(tr, kTrAFull, static_cast<unsigned>(p));
                 if (!mbar_wait(&sm.full_b[sb], phb, a.wait_ns)) { fail(sm, a); break; }
                 trace(tr, kTrMmaIssue, static_cast<unsigned>(p));
                 tc_fence_after();
-                if (N2 > 0) {
-                    tc_mma_f16_ts(tmem, at, bd, id1, acc);
-                    tc_mma_f16_ts(d2, at, bd + b2, id2, acc);
-                    tc_mma_f16_ts(tmem, at + 8u, bd + 2u, id1, 1u);
-                    tc_mma_f16_ts(d2, at + 8u, bd + b2 + 2u, id2, 1u);
-                    tc_mma_f16_ts(tmem, at + 16u, bd + 4u, id1, 1u);
-                    tc_mma_f16_ts(d2, at + 16u, bd + b2 + 4u, id2, 1u);
-                    tc_mma_f16_ts(tmem, at + 24u, bd + 6u, id1, 1u);
-                    tc_mma_f16_ts(d2, at + 24u, bd + b2 + 6u, id2, 1u);
-                } else {
-                    tc_mma_f16_ts(tmem, at, bd, id1, acc);
-                    tc_mma_f16_ts(tmem, at + 8u, bd + 2u, id1, 1u);
-                    tc_mma_f16_ts(tmem, at + 16u, bd + 4u, id1, 1u);
-                    tc_mma_f16_ts(tmem, at + 24u, bd + 6u, id1, 1u);
-                }
+                tc_mma_f16_ts(d, at, bd, idesc, acc);
+                tc_mma_f16_ts(d, at + 8u, bd + 2u, idesc, 1u);
+                tc_mma_f16_ts(d, at + 16u, bd + 4u, idesc, 1u);
+                tc_mma_f16_ts(d, at + 24u, bd + 6u, idesc, 1u);
                 tc_commit(&sm.empty_a[sa]);
                 tc_commit(&sm.empty_b[sb]);
                 acc = 1u;
                 if (++sa == AST) { sa = 0; pha ^= 1u; at = tmem + acol0; } else { at += 32u; }
-                if (++sb == R) { sb = 0; phb ^= 1u; bd = bdesc0; } else { bd += bstep; }
+                if (++sb == RB) { sb = 0; phb ^= 1u; bd = bdesc0; } else { bd += bstep; }
             }
             tc_commit(sm.done); // also taken on abort: no MMA of ours is in flight past this
         }
@@ -287,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
         const int row = q * 32 + lane;     // weight row within the tile
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         for (int p = h; p < np && !__any_sync(0xFFFFFFFFu, aborted(sm)); p += 2) {
-            const int sw = p % R, sa = p % AST;
-            if (!warp_wait(&sm.full_w[sw], (p / R) & 1, a.wait_ns)) { fail(sm, a); break; }
+            const int sw = p % RW, sa = p % AST;
+            if (!warp_wait(&sm.full_w[sw], (p / RW) & 1, a.wait_ns)) { fail(sm, a); break; }
             if (lane == 0) trace(tr, kTrWFull, static_cast<unsigned>(p));
             if (!warp_wait(&sm.empty_a[sa], ((p / AST) & 1) ^ 1, a.wait_ns)) { fail(sm, a); break; }
             const uint8_t *rec = sm.w + static_cast<size_t>(sw) * kRecordBytes;
@@ -356,10 +364,11 @@ __global__ void wait_selftest_kernel(int *status, uint64_t limit_ns)
     __syncthreads();
 }
 
-size_t gemm_smem_bytes(int T, int ring, int astages)
+size_t gemm_smem_bytes(int T, int bring, int wring, int astages)
 {
-    return 1024 + static_cast<size_t>(ring) * (static_cast<size_t>(T) * 128 + kRecordBytes) +
-           static_cast<size_t>(4 * ring + 2 * astages + 1) * 8 + 16;
+    return 1024 + static_cast<size_t>(bring) * static_cast<size_t>(T) * 128 +
+           static_cast<size_t>(wring) * kRecordBytes + static_cast<size_t>(2 * bring + 2 * wring + 2 * astages + 1) * 8 +
+           16;
 }
 
 } // namespace
@@ -394,9 +403,15 @@ bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *pl
     // sets (parity waits need a single waiter per barrier)
     best.astages = std::min(8, (512 - acol0) / 32) & ~1;
     if (best.astages < 2) return false;
-    best.ring = 8;
-    if (gemm_smem_bytes(best.T, best.ring, best.astages) > kSmemOptIn) best.ring = 4;
-    best.smem = gemm_smem_bytes(best.T, best.ring, best.astages);
+    // the deepest X-tile ring that fits next to a weight ring of 8 (or 4, 2)
+    for (int wr : {8, 4, 2}) {
+        int br = 8;
+        while (br > 2 && gemm_smem_bytes(best.T, br, wr, best.astages) > kSmemOptIn) --br;
+        if (gemm_smem_bytes(best.T, br, wr, best.astages) > kSmemOptIn) continue;
+        if (br > best.bring || (br == best.bring && wr > best.wring)) best.bring = br, best.wring = wr;
+    }
+    if (best.bring == 0) return false;
+    best.smem = gemm_smem_bytes(best.T, best.bring, best.wring, best.astages);
     if (best.smem > kSmemOptIn) return false;
     // one CTA per SM: each holds all 512 tensor-memory columns
     best.smem = std::max<size_t>(best.smem, kSmemPerSM / 2 + 1024);
@@ -426,7 +441,9 @@ cudaError_t launch_prefill(const PrefillPlan &plan, const XcastArgs &xa, const P
     a.trace_cap = tset.cap;
     a.trace_cta = tset.cta;
     void *kargs[] = {&a};
-    return launch_pdl(fn, dim3(static_cast<unsigned>(plan.rowtiles * plan.ts)), dim3(kThreads), plan.smem, s, kargs);
+    // warp 11 exists only when the tile takes two MMA threads (T >= 32)
+    const int threads = plan.T >= 32 ? kThreads : kThreads - 32;
+    return launch_pdl(fn, dim3(static_cast<unsigned>(plan.rowtiles * plan.ts)), dim3(threads), plan.smem, s, kargs);
 }
 
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t s)

@@ -218,7 +218,7 @@ def test_bitwise_deterministic(q4lib, m, n, k):
     assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (16, 1000, 2080)])
+@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (16, 1000, 2080), (100, 1000, 2080)])
 def test_weight_prefetch_mode_gives_identical_results(q4lib, oracle_mod, m, n, k):
     """Streaming W before the preceding kernel finishes changes timing only."""
     blocks = synth.q4_0_blocks(n, k, seed=81)
