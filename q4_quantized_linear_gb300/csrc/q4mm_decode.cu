@@ -605,11 +605,19 @@ bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan
     const int N = m <= 8 ? 16 : 32;
     const int64_t groups = ceil_div(n, kGroupRows);
     const int64_t np = ceil_div(k, kPairK);
-    const size_t smem_max = kSmemPerSM / 2 - 1024 - 512;   // two CTAs per SM
     const size_t smem_min = kSmemPerSM / 3 + 1024;          // never three (tensor memory)
     DecodePlan best;
     double best_cost = 1e300;
+    // Shared memory for two CTAs per SM, or, for N = 32, all of it for one
+    // (wide): the N = 32 image of X and the slices' reduction buffer leave a
+    // half-SM CTA only a shallow ring or several K passes (measured: the
+    // 151936x2560 m = 16 layer 158 -> 101 us, 9728x2560 m = 16 35.8 -> 26.4
+    // us). For N = 16 the wide plans the cost below prefers run slower
+    // (2560x9728 m = 4: 15.5 -> 29.4 us). A wide CTA leaves no room for the
+    // next call's, but K passes cost more than that overlap does.
+    for (int wide = 0; wide <= (N == 32 ? 1 : 0); ++wide)
     for (int S = 1; S <= kMaxSlices && S <= np; ++S) {
+        const size_t smem_max = wide ? kSmemOptIn - 1024 : kSmemPerSM / 2 - 1024 - 512;
         for (int64_t passes = 1; passes <= np; ++passes) {
             const int64_t ppp = ceil_div(np, passes);        // pairs per pass
             if (ppp < S) break;
@@ -626,8 +634,10 @@ bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan
             }
             if (ring == 0) continue;                          // more passes: smaller slices
             const size_t smem = std::max(decode_smem(N, static_cast<int>(P), S, m, ring), smem_min);
-            // one CTA per SM (room for the next call to overlap) or two
-            for (int per = 1; per <= 2; ++per) {
+            // a wide CTA holds its SM alone; otherwise one CTA per SM (room
+            // for the next call to overlap) or two
+            if (wide && smem <= kSmemPerSM / 2 - 1024 - 512) break;      // not wide after all
+            for (int per = 1; per <= (wide ? 1 : 2); ++per) {
                 const int64_t clusters = std::min<int64_t>(groups, (per * sm_count) / S);
                 if (clusters < 1) continue;
                 const int64_t tiles_per = ceil_div(groups, clusters);
