@@ -1,9 +1,11 @@
 // q4mm_api.cu -- the C ABI of libq4mm (declared in include/q4mm.h): argument
 // validation, per-device state, workspace handling and dispatch between the
-// decode kernel (m <= 16) and the tensor-core prefill kernels (m > 16).
+// CUDA-core GEMV kernel (m <= 2 by default), the tensor-core decode kernel
+// (up to m = 16) and the tensor-core prefill kernels (m > 16).
 //
-// The dispatch point follows golem, "Reading a prompt on the card": the
-// mat-vec is built up to sixteen columns and tiled products take over beyond.
+// The decode/prefill dispatch point follows golem, "Reading a prompt on the
+// card": the mat-vec is built up to sixteen columns and tiled products take
+// over beyond.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -26,6 +28,7 @@ constexpr int64_t kDecodeMaxM = 16;
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 std::atomic<int> g_prefetch_w{0};
+std::atomic<int> g_gemv_max_m{2};
 std::mutex g_trace_mutex;
 TraceSettings g_trace;
 
@@ -158,9 +161,7 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     const uint64_t wait_ns = g_wait_ns.load();
 
     if (m <= kDecodeMaxM) {
-        // the decode path needs no scratch: K slices meet in cluster shared memory
-        DecodePlan plan;
-        if (!plan_decode(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
+        // the decode paths need no scratch: K slices meet in cluster shared memory
         DecodeArgs a{};
         a.W = static_cast<const uint8_t *>(W);
         a.X = X;
@@ -176,6 +177,13 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.np = static_cast<int>(ceil_div(k, kPairK));
         a.groups = static_cast<int>(ceil_div(n, kGroupRows));
         a.prefetch_w = g_prefetch_w.load();
+        if (m <= g_gemv_max_m.load()) {
+            GemvPlan gp;
+            if (!plan_gemv(m, k, n, dev.sm_count, &gp)) return Q4_ERR_INVALID_ARG;
+            return map_cuda(launch_gemv(gp, a, s));
+        }
+        DecodePlan plan;
+        if (!plan_decode(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
         return map_cuda(launch_decode(plan, a, s));
     }
 
@@ -401,6 +409,13 @@ Q4MM_API int q4_set_wait_limit_ns(uint64_t ns)
 Q4MM_API int q4_set_weight_prefetch(int enable)
 {
     g_prefetch_w.store(enable ? 1 : 0);
+    return Q4_OK;
+}
+
+Q4MM_API int q4_set_gemv_max_m(int max_m)
+{
+    if (max_m < 0 || max_m > kGemvMaxM) return Q4_ERR_INVALID_ARG;
+    g_gemv_max_m.store(max_m);
     return Q4_OK;
 }
 

@@ -1,0 +1,536 @@
+// q4mm_gemv.cu -- the CUDA-core kernel for the narrowest decode calls, m = 1
+// to 4 token rows: the decode step (m = 1) and small continuous batches
+// (golem, "Several conversations, one pass"; golem-server, "Several
+// conversations, in one pass"). The pages bound this case by the weight read
+// (golem: two columns cost what one did; goinfer ch. 10, "What the kernels
+// are": the quantised mat-vec is the decode workhorse), so the design goal is
+// to consume a packed record at the rate one SM's share of HBM delivers it
+// with as few instructions as possible.
+//
+// Arithmetic. A weight is (q - 8) * d. One lop3 per weight ORs the nibble,
+// left where it lies in its 32-bit word (bit offset s <= 16), into the fp32
+// pattern of 2^23, giving exactly 2^23 + q * 2^s. One packed fp32 FMA per two
+// weights, v * 2^-s - (2^(23-s) + 8), gives (q - 8) exactly. A second packed
+// FMA per two weights and token multiplies by x, read as fp32 and never
+// rounded, and accumulates in fp32 over the block's 32 elements; the block
+// sum is then scaled by d (fp16, exact in fp32) into the row's fp32 partial.
+// About 2.25 instructions per weight for m = 1, against the ~4.5 that one
+// SM's issue rate allows at three quarters of HBM bandwidth; the tensor core
+// would spend its MMA issue on columns that m = 1 leaves empty.
+//
+// Work split (the decode kernel's): 128-row groups and S slices of K; the S
+// CTAs of a thread-block cluster hold the S slices of the groups c, c + C, ...
+// of their cluster c, and slices meet in the first CTA's shared memory
+// (DSMEM), summed in slice order, so results are bitwise reproducible and no
+// global scratch is used.
+//
+// Warp roles: eight warps per CTA, all alike (two CTAs fit on an SM).
+// Warp c owns the records u = c (mod 8) of the CTA's sequence (its groups x
+// its pairs, in that order) and the ring slots they pass through, R / 8 of
+// them: lane 0 refills a slot with a 1-D bulk copy of the record R places
+// ahead as soon as the warp has read it, so every barrier has one waiter and
+// no copy is in flight when the CTA exits. Lane l owns rows l, l + 32, l + 64
+// and l + 96 of a record: every shared-memory load is 512 contiguous bytes
+// per warp (conflict-free) and every X value a thread loads (a broadcast,
+// L1-resident) serves four rows. At the end of a group each warp leaves its
+// partial rows in shared memory; one group later (so that no warp waits for
+// the slowest), warp c sums the eight partials of rows 16c .. 16c + 15 in
+// order, and then the cluster's slices of those rows, and writes Y. Every
+// wait is bounded and warp-uniform.
+#include <algorithm>
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "q4mm_device.cuh"
+#include "q4mm_internal.h"
+
+namespace q4 {
+namespace {
+
+constexpr int kErrTimeout = 5;      // Q4_ERR_DEVICE_TIMEOUT
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSliceRows = kGroupRows / kWarps;   // rows of a group each warp reduces
+constexpr int kMaxSlices = 8;
+constexpr int kMaxRing = 32;
+
+struct GSmem {
+    uint8_t *w;          // [R] records
+    float *part;         // [2][kWarps][M][128] warps' partial rows of a group
+    float *red;          // [2][S - 1][M][128] other slices' rows (first CTA of the cluster)
+    uint64_t *full_w;    // [R]
+    uint64_t *gfull, *gfree;        // [2] partials of a group parity written / summed
+    uint64_t *red_full, *red_free;  // [2][kWarps] a row slice's other slices landed / slot free
+};
+
+__device__ __forceinline__ void fail(const DecodeArgs &a) { record_status(a.status, kErrTimeout); }
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, limit_ns)) != 0;
+}
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    return __all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar, parity, limit_ns)) != 0;
+}
+
+// (w & mask) | bits of 2^23: the nibble under `mask` (at bit s <= 16) read as
+// the fp32 value 2^23 + q * 2^s, exactly.
+__device__ __forceinline__ float nib_f32(uint32_t w, uint32_t mask)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(0x4B000000u));
+    return __uint_as_float(r);
+}
+
+// The eight weights of one word of split-half nibbles (bytes 4c..4c+3 of a
+// block's qs, element base e = 4c; byte i holds element i low, i + 16 high)
+// as exact fp32 (q - 8), paired like the X values they multiply:
+//   f[0] = (e, e+1)  f[1] = (e+2, e+3)  f[2] = (e+16, e+17)  f[3] = (e+18, e+19).
+// Bit offsets in w: e 0, e+16 4, e+1 8, e+17 12, e+2 16, e+18 20, e+3 24,
+// e+19 28; the last three are read from w >> 12 at 8, 12, 16.
+// Multipliers and addends of the conversion, one pair per f[] entry, held in
+// registers for the whole kernel.
+struct Conv {
+    float2 m[4], c[4];
+};
+
+// A float pair the compiler must keep in registers as it is (no constant
+// folding or rematerialisation).
+__device__ __forceinline__ float2 reg_pair(float a, float b)
+{
+    float x, y;
+    asm volatile("mov.b32 %0, %2;\n\tmov.b32 %1, %3;" : "=f"(x), "=f"(y) : "f"(a), "f"(b));
+    return make_float2(x, y);
+}
+
+__device__ __forceinline__ Conv make_conv()
+{
+    Conv k;
+    k.m[0] = reg_pair(1.0f, 0x1p-8f);
+    k.c[0] = reg_pair(-(0x1p23f + 8.0f), -(0x1p15f + 8.0f));
+    k.m[1] = reg_pair(0x1p-16f, 0x1p-12f);
+    k.c[1] = reg_pair(-(0x1p7f + 8.0f), -(0x1p11f + 8.0f));
+    k.m[2] = reg_pair(0x1p-4f, 0x1p-12f);
+    k.c[2] = reg_pair(-(0x1p19f + 8.0f), -(0x1p11f + 8.0f));
+    k.m[3] = reg_pair(0x1p-8f, 0x1p-16f);
+    k.c[3] = reg_pair(-(0x1p15f + 8.0f), -(0x1p7f + 8.0f));
+    return k;
+}
+
+__device__ __forceinline__ void unpack_word_f32(uint32_t w, const Conv &k, float2 f[4])
+{
+    const uint32_t w2 = w >> 12;
+    const float2 a = make_float2(nib_f32(w, 0x0000Fu), nib_f32(w, 0x00F00u));    // e   (s 0),  e+1  (s 8)
+    const float2 b = make_float2(nib_f32(w, 0xF0000u), nib_f32(w2, 0x0F000u));   // e+2 (s 16), e+3  (s 12)
+    const float2 c = make_float2(nib_f32(w, 0x000F0u), nib_f32(w, 0x0F000u));    // e+16 (s 4), e+17 (s 12)
+    const float2 d = make_float2(nib_f32(w2, 0x00F00u), nib_f32(w2, 0xF0000u));  // e+18 (s 8), e+19 (s 16)
+    f[0] = __ffma2_rn(a, k.m[0], k.c[0]);
+    f[1] = __ffma2_rn(b, k.m[1], k.c[1]);
+    f[2] = __ffma2_rn(c, k.m[2], k.c[2]);
+    f[3] = __ffma2_rn(d, k.m[3], k.c[3]);
+}
+
+__device__ __forceinline__ uint32_t lds32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+    return v;
+}
+
+// One block (32 elements) of the record for the thread's four rows: adds
+// d * sum_i (q_i - 8) x[t][kb + i] into yp[r][t]. A row's 16 bytes of
+// nibbles are one 16-byte load (lanes 16 bytes apart: conflict-free). M == 1
+// keeps two accumulator pairs per row for a shorter dependency chain.
+template <int M>
+__device__ __forceinline__ void gemv_block(const uint8_t *qs, uint32_t dsh, const uint32_t sc[4],
+                                           const float *const xr[M], int kb, int lane, const Conv &kc,
+                                           float yp[4][M])
+{
+    constexpr int A = M == 1 ? 2 : 1;
+    float2 acc[4][M][A];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < M; ++t)
+#pragma unroll
+            for (int z = 0; z < A; ++z) acc[r][t][z] = make_float2(0.0f, 0.0f);
+    uint4 q[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) q[r] = lds128(qs + 16 * (lane + 32 * r));
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+        uint32_t qw[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) qw[r] = wd == 0 ? q[r].x : wd == 1 ? q[r].y : wd == 2 ? q[r].z : q[r].w;
+        float4 xl[M], xh[M];
+#pragma unroll
+        for (int t = 0; t < M; ++t) {
+            xl[t] = __ldg(reinterpret_cast<const float4 *>(xr[t] + kb + 4 * wd));
+            xh[t] = __ldg(reinterpret_cast<const float4 *>(xr[t] + kb + 16 + 4 * wd));
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float2 f[4];
+            unpack_word_f32(qw[r], kc, f);
+#pragma unroll
+            for (int t = 0; t < M; ++t) {
+                acc[r][t][0] = __ffma2_rn(f[0], make_float2(xl[t].x, xl[t].y), acc[r][t][0]);
+                acc[r][t][A - 1] = __ffma2_rn(f[1], make_float2(xl[t].z, xl[t].w), acc[r][t][A - 1]);
+                acc[r][t][0] = __ffma2_rn(f[2], make_float2(xh[t].x, xh[t].y), acc[r][t][0]);
+                acc[r][t][A - 1] = __ffma2_rn(f[3], make_float2(xh[t].z, xh[t].w), acc[r][t][A - 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float d = __half2float(__ushort_as_half(static_cast<unsigned short>((sc[r] >> dsh) & 0xFFFFu)));
+#pragma unroll
+        for (int t = 0; t < M; ++t) {
+            float s = acc[r][t][0].x + acc[r][t][0].y;
+            if (A == 2) s += acc[r][t][A - 1].x + acc[r][t][A - 1].y;
+            yp[r][t] = fmaf(d, s, yp[r][t]);
+        }
+    }
+}
+
+// Issue the bulk copy of the CTA's record (group i of its cluster, pair j of
+// its slice) into ring slot s. Lane 0 of the slot's warp only.
+__device__ __forceinline__ void load_record(const DecodeArgs &a, const GSmem &sm, int i, int j, int s, int G0,
+                                            int p0, uint64_t pol)
+{
+    const int64_t rec = static_cast<int64_t>(G0 + i * a.clusters) * a.np + p0 + j;
+    mbar_arrive_expect_tx(&sm.full_w[s], kRecordBytes);
+    bulk_g2s_hint(sm.w + static_cast<size_t>(s) * kRecordBytes, a.W + rec * kRecordBytes, kRecordBytes,
+                  &sm.full_w[s], pol);
+}
+
+// Advance a (group, pair) position of the CTA's record sequence by one step
+// of a warp (kWarps records).
+__device__ __forceinline__ void step_pos(int &i, int &j, int P)
+{
+    j += kWarps;
+    while (j >= P) j -= P, ++i;
+}
+
+// Sum the eight warps' partials of group g for this warp's rows, then meet
+// the cluster's other slices of them and write Y (first CTA) or send them
+// there. Lane l handles row 16 c + (l & 15) and tokens t = l / 16, + 2, ...
+template <int M>
+__device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &sm, int g, int c, int lane, int rank,
+                                             int G0, const int yrow[M])
+{
+    const int S = a.S;
+    const int tb = g & 1;
+    const uint32_t par = static_cast<uint32_t>((g >> 1) & 1);
+    if (!warp_wait(&sm.gfull[tb], par, a.wait_ns)) return false;
+    const int row = c * kSliceRows + (lane & (kSliceRows - 1));
+    const int t0 = lane >> 4;
+    float y[(M + 1) / 2];
+#pragma unroll
+    for (int h = 0; h < (M + 1) / 2; ++h) {
+        const int t = t0 + 2 * h;
+        float v = 0.0f;
+        if (t < M)
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += sm.part[((tb * kWarps + w) * M + t) * kGroupRows + row];
+        y[h] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.gfree[tb]);
+    const int64_t grow = static_cast<int64_t>(G0 + g * a.clusters) * kGroupRows + row;
+    if (rank > 0) {
+        // this slice's rows into the first CTA's slot tb, then signal it
+        if (g >= 2 && !warp_wait_cluster(&sm.red_free[tb * kWarps + c], par ^ 1u, a.wait_ns)) return false;
+        const uint32_t dst = mapa_shared(smem_u32(sm.red), 0u) +
+                             static_cast<uint32_t>(((((tb * (S - 1) + rank - 1) * M) * kGroupRows) + row) * 4);
+#pragma unroll
+        for (int h = 0; h < (M + 1) / 2; ++h) {
+            const int t = t0 + 2 * h;
+            if (t < M) st_cluster_f32(dst + static_cast<uint32_t>(t * kGroupRows * 4), y[h]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_full[tb * kWarps + c]), 0u));
+    } else {
+        if (S > 1 && !warp_wait_cluster(&sm.red_full[tb * kWarps + c], par, a.wait_ns)) return false;
+        if (grow < a.n) {
+#pragma unroll
+            for (int h = 0; h < (M + 1) / 2; ++h) {
+                const int t = t0 + 2 * h;
+                if (t < M && t < a.m) {
+                    float v = y[h];
+                    for (int r = 1; r < S; ++r) v += sm.red[((tb * (S - 1) + r - 1) * M + t) * kGroupRows + row];
+                    a.Y[static_cast<int64_t>(yrow[t]) * a.ldy + grow] = v;
+                }
+            }
+        }
+        if (S > 1) {
+            __syncwarp();
+            if (lane == 0)
+                for (int r = 1; r < S; ++r)
+                    mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_free[tb * kWarps + c]), static_cast<uint32_t>(r)));
+        }
+    }
+    return true;
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, c = tid >> 5, lane = tid & 31;
+    const int S = a.S;
+    const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int G0 = blockIdx.x / S;                  // first group of this cluster
+    const int ntiles = G0 < a.groups ? (a.groups - 1 - G0) / a.clusters + 1 : 0;
+    const int p0 = rank * a.pbase + min(rank, a.prem);
+    const int P = a.pbase + (rank < a.prem ? 1 : 0);
+    const int total = ntiles * P;                    // records this CTA streams
+    const int R = a.ring;
+
+    GSmem sm;
+    sm.w = smem_raw;
+    sm.part = reinterpret_cast<float *>(sm.w + static_cast<size_t>(R) * kRecordBytes);
+    sm.red = sm.part + 2 * kWarps * M * kGroupRows;
+    const int red_floats = S > 1 ? 2 * (S - 1) * M * kGroupRows : 0;
+    sm.full_w = reinterpret_cast<uint64_t *>(sm.red + red_floats);
+    sm.gfull = sm.full_w + R;
+    sm.gfree = sm.gfull + 2;
+    sm.red_full = sm.gfree + 2;
+    sm.red_free = sm.red_full + 2 * kWarps;
+
+    if (tid == 0) {
+        for (int i = 0; i < R; ++i) mbar_init(&sm.full_w[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.gfull[i], kWarps);
+            mbar_init(&sm.gfree[i], kWarps);
+        }
+        for (int i = 0; i < 2 * kWarps; ++i) {
+            mbar_init(&sm.red_full[i], S > 1 ? S - 1 : 1);
+            mbar_init(&sm.red_free[i], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // The next kernel in the stream may be scheduled now: it waits for this
+    // one to complete before it reads anything this one writes.
+    pdl_launch_dependents();
+    if (S > 1) cluster_sync(); // every CTA's barriers initialised before any remote arrive
+
+    // Warp c reads the records u = c, c + 8, ... of the sequence (group u / P,
+    // pair u % P), record u through slot u % R. Positions advance by steps,
+    // without divisions: (ci, cj) the next record to read, in slot s of
+    // phase ph; (fi, fj) the next record to fetch, R places ahead.
+    const Conv kc = make_conv();
+    const uint64_t pol = policy_evict_first();
+    // Weights may stream before the preceding kernel has finished only when
+    // the caller declared them read-only.
+    if (!a.prefetch_w) pdl_wait();
+    int ci = c / max(P, 1), cj = c - ci * max(P, 1);
+    int fi = ci, fj = cj;
+    for (int u = c; u < R; u += kWarps) {
+        if (lane == 0 && fi < ntiles) load_record(a, sm, fi, fj, u, G0, p0, pol);
+        step_pos(fi, fj, P);
+    }
+    __syncwarp();
+    pdl_wait();                                       // X, Y and the slot rows are the preceding kernel's
+    const float *xr[M];
+    int yrow[M];
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+        yrow[t] = t < a.m ? (a.rows ? __ldg(a.rows + t) : t) : 0;
+        xr[t] = a.X + static_cast<int64_t>(yrow[t]) * a.ldx;
+    }
+
+    bool ok = true;
+    int s = c;
+    uint32_t ph = 0;
+    int pending = c;                                  // first of this warp's records not yet read
+    for (int g = 0; g < ntiles && ok; ++g) {
+        const int tb = g & 1;
+        float yp[4][M];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < M; ++t) yp[r][t] = 0.0f;
+        for (; ci == g; step_pos(ci, cj, P)) {
+            if (!warp_wait(&sm.full_w[s], ph, a.wait_ns)) { ok = false; break; }
+            const uint8_t *rec = sm.w + static_cast<size_t>(s) * kRecordBytes;
+            uint32_t sc[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[r] = lds32(rec + kRecScaleOff + 4 * (lane + 32 * r));
+            const int b0 = 2 * (p0 + cj);
+            gemv_block<M>(rec + kRecQs0Off, 0, sc, xr, 32 * b0, lane, kc, yp);
+            if (b0 + 1 < a.nb) gemv_block<M>(rec + kRecQs1Off, 16, sc, xr, 32 * (b0 + 1), lane, kc, yp);
+            // Every lane has its values of the slot in registers: refill it
+            // with the record R places ahead (same warp, same slot).
+            __syncwarp();
+            if (lane == 0 && fi < ntiles) load_record(a, sm, fi, fj, s, G0, p0, pol);
+            step_pos(fi, fj, P);
+            pending += kWarps;
+            s += kWarps;
+            if (s >= R) s -= R, ph ^= 1u;
+        }
+        if (!ok) break;
+        if (g >= 2 && !warp_wait(&sm.gfree[tb], ((g >> 1) & 1) ^ 1u, a.wait_ns)) { ok = false; break; }
+        float *pp = sm.part + (tb * kWarps + c) * M * kGroupRows;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < M; ++t) pp[t * kGroupRows + lane + 32 * r] = yp[r][t];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.gfull[tb]);
+        if (g >= 1 && !reduce_group<M>(a, sm, g - 1, c, lane, rank, G0, yrow)) { ok = false; break; }
+    }
+    if (ok && ntiles > 0) ok = reduce_group<M>(a, sm, ntiles - 1, c, lane, rank, G0, yrow);
+    if (!ok) {
+        fail(a);
+        // A warp that gave up may still have copies landing in its slots
+        // (the records after the last one it read): wait for them, bounded,
+        // so that none lands after the CTA has exited.
+        for (int u = pending; u < total && u < pending + R; u += kWarps)
+            if (!mbar_wait(&sm.full_w[u % R], (u / R) & 1, a.wait_ns)) break;
+        __syncwarp();
+    }
+
+    // every CTA of the cluster stays until the others are done with its
+    // shared memory and barriers
+    if (S > 1) cluster_sync();
+}
+
+size_t gemv_smem(int M, int S, int ring)
+{
+    const size_t part = static_cast<size_t>(2 * kWarps) * M * kGroupRows * 4;
+    const size_t red = S > 1 ? static_cast<size_t>(2 * (S - 1)) * M * kGroupRows * 4 : 0;
+    const size_t bars = static_cast<size_t>(ring + 4 + 4 * kWarps) * 8;
+    return static_cast<size_t>(ring) * kRecordBytes + part + red + bars;
+}
+
+const void *gemv_fn(int M)
+{
+    switch (M) {
+    case 1: return reinterpret_cast<const void *>(&gemv_kernel<1>);
+    case 2: return reinterpret_cast<const void *>(&gemv_kernel<2>);
+    case 3: return reinterpret_cast<const void *>(&gemv_kernel<3>);
+    default: return reinterpret_cast<const void *>(&gemv_kernel<4>);
+    }
+}
+
+// Largest number of clusters of S CTAs of the M-token kernel with `smem`
+// bytes of dynamic shared memory that the current device can hold at once
+// (clusters live inside one GPC, so this is less than the SM count allows
+// whenever S does not divide a GPC's SMs). Cached per (device, M, S, smem).
+int max_active_clusters(int M, int S, size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const auto key = std::make_tuple(dev, M, S, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const void *fn = gemv_fn(M);
+    int n = 0;
+    if (set_max_smem(fn, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(S));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(S);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache.emplace(key, n);
+    return n;
+}
+
+} // namespace
+
+// Choose the cluster size S (K slices per 128-row group), the number of
+// persistent clusters and the ring depth. Candidates per S: the deepest ring
+// that fits one CTA's shared memory, and the deepest that leaves room for a
+// second CTA on the SM (the next call's, or this call's). The number of
+// clusters is capped by what the device holds at once (a second wave would
+// double the time). Cost, in record times of one SM's share of HBM: the
+// busiest SM's records at the rate its CTAs sustain, plus per-group and
+// per-slice overheads, plus the start-up that cannot overlap the preceding
+// call when no SM has room left for the next call's CTA.
+bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
+{
+    if (m < 1 || m > kGemvMaxM || sm_count < 1) return false;
+    const int M = static_cast<int>(m);
+    const int64_t groups = ceil_div(n, kGroupRows);
+    const int64_t np = ceil_div(k, kPairK);
+    const double total = static_cast<double>(groups * np);
+    const size_t half = kSmemPerSM / 2 - 1024;
+    GemvPlan best;
+    double best_cost = 1e300;
+    for (int S = 1; S <= kMaxSlices && S <= np; ++S) {
+        for (int two = 0; two <= 1; ++two) {
+            const size_t limit = two ? half : kSmemOptIn;
+            int ring = 0;
+            for (int r = kMaxRing; r >= kWarps && ring == 0; r -= kWarps)
+                if (gemv_smem(M, S, r) <= limit) ring = r;
+            if (ring == 0) continue;
+            const size_t smem = gemv_smem(M, S, ring);
+            const bool two_fit = smem <= half;
+            if (!two && two_fit) continue;             // the same plan as two = 1
+            const int64_t cmax = max_active_clusters(M, S, smem);
+            if (cmax < 1) continue;
+            const int64_t clusters = std::min<int64_t>(groups, cmax);
+            const int64_t tiles = ceil_div(groups, clusters);
+            const int64_t P = ceil_div(np, S);
+            const int64_t ctas = clusters * S;
+            const int per_sm = ctas > sm_count ? 2 : 1;
+            const double rate = per_sm == 2 ? 1.0 : (two_fit ? 0.9 : 0.8);
+            const double stream = std::max(static_cast<double>(tiles * P * per_sm) / rate, total / sm_count);
+            const double no_overlap = (!two_fit || per_sm == 2) ? 15.0 : 0.0;
+            const double cost = stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 2.0 : 0.0) + no_overlap;
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.M = M;
+                best.S = S;
+                best.clusters = static_cast<int>(clusters);
+                best.ctas = static_cast<int>(ctas);
+                best.ring = ring;
+                best.smem = smem;
+            }
+        }
+    }
+    if (best.ctas == 0) return false;
+    *plan = best;
+    return true;
+}
+
+cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, cudaStream_t s)
+{
+    const void *fn = gemv_fn(plan.M);
+    cudaError_t e = set_max_smem(fn, plan.smem);
+    if (e != cudaSuccess) return e;
+    DecodeArgs a = args;
+    a.pass_p0 = 0;
+    a.S = plan.S;
+    a.pbase = args.np / plan.S;
+    a.prem = args.np % plan.S;
+    a.clusters = plan.clusters;
+    a.ring = plan.ring;
+    a.accumulate = 0;
+    a.xs_bytes = 0;
+    void *kargs[] = {&a};
+    return launch_pdl(fn, dim3(plan.ctas), dim3(kThreads), plan.smem, s, kargs, plan.S);
+}
+
+} // namespace q4

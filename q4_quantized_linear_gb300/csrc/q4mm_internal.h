@@ -99,6 +99,23 @@ struct DecodePlan {
 bool plan_decode(int64_t m, int64_t k, int64_t n, int sm_count, DecodePlan *plan);
 cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaStream_t s);
 
+// ------------------------------------------------------------------ gemv --
+
+// Widest call the CUDA-core GEMV kernel is built for.
+constexpr int kGemvMaxM = 4;
+
+struct GemvPlan {
+    int M = 1;             // token rows (the kernel instance)
+    int S = 1;             // K slices = cluster size
+    int clusters = 0;      // persistent clusters: cluster c owns groups c, c + clusters, ...
+    int ctas = 0;          // clusters x S
+    int ring = 8;          // weight-record ring depth (multiple of 8)
+    size_t smem = 0;
+};
+
+bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan);
+cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, cudaStream_t s);
+
 // --------------------------------------------------------------- prefill --
 
 struct PrefillArgs {

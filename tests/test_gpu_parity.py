@@ -57,6 +57,60 @@ def test_decode_parity(q4lib, oracle_mod, m, n, k):
     assert_parity(Y, Yr, B, m, f"decode m={m} n={n} k={k}")
 
 
+@pytest.fixture
+def tensor_decode_kernel(q4lib):
+    """Send every m <= 16 to the tensor-core decode kernel for one test."""
+    q4lib.q4_set_gemv_max_m(0)
+    yield
+    q4lib.q4_set_gemv_max_m(2)
+
+
+@pytest.fixture
+def gemv_kernel_to_4(q4lib):
+    """Send every m <= 4 to the CUDA-core GEMV kernel for one test."""
+    q4lib.q4_set_gemv_max_m(4)
+    yield
+    q4lib.q4_set_gemv_max_m(2)
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4])
+@pytest.mark.parametrize("n,k", SHAPES)
+def test_tensor_decode_kernel_small_m(q4lib, oracle_mod, tensor_decode_kernel, m, n, k):
+    """The smallest m normally run on the CUDA-core GEMV kernel; the
+    tensor-core decode kernel must meet the same bound there."""
+    blocks = synth.q4_0_blocks(n, k, seed=1000 + n)
+    X = synth.activations(m, k, seed=2000 + m)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, f"tensor decode m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 4])
+@pytest.mark.parametrize("n,k", SHAPES)
+def test_gemv_kernel_parity(q4lib, oracle_mod, gemv_kernel_to_4, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=1000 + n)
+    X = synth.activations(m, k, seed=2000 + m)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, f"gemv m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (2, 14336, 4096), (3, 2560, 9728), (4, 151936, 256)])
+def test_gemv_kernel_is_fp32_accurate(q4lib, oracle_mod, gemv_kernel_to_4, m, n, k):
+    """The CUDA-core kernel forms (q - 8) exactly and multiplies fp32 X
+    unrounded: its error is a few fp32 roundings of B, far inside the decode
+    bound (checked at 1/50 of it)."""
+    blocks = synth.q4_0_blocks(n, k, seed=91)
+    X = synth.activations(m, k, seed=92)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n).astype(np.float64)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    ratio = float((np.abs(Y - Yr) / (2e-5 * B + 1e-7)).max())
+    assert ratio <= 1.0, f"m={m}: max err / (2e-5 B + 1e-7) = {ratio:.3g}"
+
+
 @pytest.mark.parametrize("m", [17, 31, 64, 100, 257, 300])
 @pytest.mark.parametrize("n,k", [(64, 64), (65, 96), (200, 1056), (513, 2080), (260, 640)])
 def test_prefill_parity(q4lib, oracle_mod, m, n, k):
@@ -156,7 +210,7 @@ def test_m_zero_is_a_no_op(q4lib):
     assert torch.all(Y == 3.0)
 
 
-@pytest.mark.parametrize("m", [1, 7, 16, 17, 100])
+@pytest.mark.parametrize("m", [1, 2, 4, 7, 16, 17, 100])
 def test_all_eights_give_exact_zero(q4lib, m):
     n, k = 130, 640
     blocks = synth.q4_0_blocks(n, k, seed=21)
@@ -166,7 +220,7 @@ def test_all_eights_give_exact_zero(q4lib, m):
     assert np.all(Y == 0.0)
 
 
-@pytest.mark.parametrize("m", [1, 5, 16, 17, 64, 300])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 16, 17, 64, 300])
 def test_exact_integer_case_is_bit_exact(q4lib, oracle_mod, m):
     """Power-of-two scales and small integer X: every partial sum is an exact
     integer times a power of two, on both paths, so the results are equal."""
@@ -183,7 +237,7 @@ def test_exact_integer_case_is_bit_exact(q4lib, oracle_mod, m):
     assert np.array_equal(Y.astype(np.float64), Yr)
 
 
-@pytest.mark.parametrize("m", [1, 16, 17, 64])
+@pytest.mark.parametrize("m", [1, 3, 5, 16, 17, 64])
 def test_nonfinite_x_propagates(q4lib, oracle_mod, m):
     n, k = 100, 256
     blocks = synth.q4_0_blocks(n, k, seed=41)
@@ -196,7 +250,7 @@ def test_nonfinite_x_propagates(q4lib, oracle_mod, m):
     assert_parity(Y, Yr, B, m, "non-finite X")
 
 
-@pytest.mark.parametrize("m", [3, 33])
+@pytest.mark.parametrize("m", [3, 6, 33])
 def test_zero_and_negative_scales(q4lib, oracle_mod, m):
     n, k = 96, 512
     blocks = synth.q4_0_blocks(n, k, seed=51)
@@ -208,7 +262,8 @@ def test_zero_and_negative_scales(q4lib, oracle_mod, m):
     assert_parity(Y, Yr, B, m, "zero/negative scales")
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (16, 14336, 4096), (540, 9728, 2560)])
+@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (2, 2560, 9728), (4, 2560, 9728), (8, 2560, 9728),
+                                   (16, 14336, 4096), (540, 9728, 2560)])
 def test_bitwise_deterministic(q4lib, m, n, k):
     blocks = synth.q4_0_blocks(n, k, seed=61)
     X = synth.activations(m, k, seed=62)
@@ -218,7 +273,8 @@ def test_bitwise_deterministic(q4lib, m, n, k):
     assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (16, 1000, 2080), (100, 1000, 2080)])
+@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (8, 2560, 9728), (16, 1000, 2080),
+                                   (100, 1000, 2080)])
 def test_weight_prefetch_mode_gives_identical_results(q4lib, oracle_mod, m, n, k):
     """Streaming W before the preceding kernel finishes changes timing only."""
     blocks = synth.q4_0_blocks(n, k, seed=81)
