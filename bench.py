@@ -72,6 +72,15 @@ def weight_bytes(n, k):
     return n * (k // 32) * 18
 
 
+def decode_kernel_name(m):
+    """The kernel the library's automatic dispatch runs for m token rows."""
+    if m > 16:
+        return "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)"
+    if m <= 2:
+        return "gemv_kernel (q4mm_gemv.cu, CUDA cores)"
+    return "mmv_kernel (q4mm_mmv.cu, warp-level MMA)"
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -433,7 +442,7 @@ def native(args):
         },
         "roofline": {
             "bound": "tensor" if tensor else "hbm",
-            "kernel": "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)" if tensor else "decode_kernel (q4mm_decode.cu)",
+            "kernel": decode_kernel_name(m),
             "achieved": achieved,
             "peak": peak,
             "unit": unit,

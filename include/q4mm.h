@@ -115,18 +115,16 @@ Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
  *   X: device fp32 [m x k] row-major, 16-byte aligned.
  *   Y: device fp32 [m x n] row-major, overwritten (no accumulate); 4-byte aligned.
  *   m >= 0 (m == 0 does nothing), n >= 1, k >= 32, k % 32 == 0.
- * Precision: calls that take the CUDA-core GEMV kernel (m <= 2 by default,
- * see q4_set_gemv_max_m) form each weight (q - 8) exactly in fp32, multiply
- * by X as given (fp32, never rounded) and accumulate in fp32, a block's 32
- * products first, then d times the block sum: |Y - Y_exact| is a few fp32
- * rounding errors of B = sum_c |X[t][c] * W[j][c]|. The other calls with
- * m <= 16 (the tensor-core decode kernel) round each weight (q - 8) * d once
- * to fp16 (relative error <= 2^-11), scale each X row by a power of two and
- * split it into two fp16 terms (22 significant bits relative to the row's
- * largest |x|), and accumulate in fp32. Every m <= 16 meets |Y - Y_exact| <=
- * 1e-3 * B + 1e-5 (the tensor-core kernel for scales |d| <= 4096, as larger
- * scales overflow fp16, and rows whose nonzero |x| do not span more than
- * about 2^20). For m > 16 X is rounded to bf16 (nearest even), each weight is
+ * Precision (m <= 16, see q4_set_decode_kernel for which kernel runs):
+ * the warp-MMA kernel forms each weight's (q - 8) exactly, scales each
+ * 32-element block of an X row by a power of two and splits it into two fp16
+ * terms (22 significant bits relative to the block's largest |x|), and
+ * accumulates in fp32, applying d in fp32 per block; the CUDA-core kernel
+ * uses (q - 8) exactly and X unrounded, in fp32; the tcgen05 kernel rounds
+ * each weight (q - 8) * d once to fp16 (relative error <= 2^-11, scales |d|
+ * <= 4096) and splits each X row, scaled by a power of two, into two fp16
+ * terms. Each meets |Y - Y_exact| <= 1e-3 * B + 1e-5, B = sum_c |X[t][c] *
+ * W[j][c]|. For m > 16 X is rounded to bf16 (nearest even), each weight is
  * the exact (q - 8) times d rounded to bf16, rounded to bf16 (relative error
  * <= 2^-8), and the tensor cores accumulate in fp32: |Y - Y_exact| <= 1e-2 *
  * B + 1e-4. NaN and infinity in X propagate as in IEEE arithmetic.
@@ -218,15 +216,26 @@ Q4MM_API int q4_set_wait_limit_ns(uint64_t ns);
  * event before the first matmul). Applies to launches made after the call. */
 Q4MM_API int q4_set_weight_prefetch(int enable);
 
-/* Largest m that runs on the CUDA-core GEMV kernel, 0..4 (default 2; 0 sends
- * every m <= 16 to the tensor-core decode kernel). The pages bound decode by
- * the weight read (golem, "Qwen3.8 drafts its own next token"); for the
- * narrowest calls one SM's CUDA cores keep up with its share of HBM with
- * fewer instructions than the tensor-core path's dequantise-to-TMEM-and-MMA
- * sequence. Both kernels meet the decode tolerance; this is a performance
- * setting for the whole process, applying to launches made after the call.
- * Values outside 0..4 are refused with Q4_ERR_INVALID_ARG. */
-Q4MM_API int q4_set_gemv_max_m(int max_m);
+/* Decode kernels (m <= 16). Every one meets the decode tolerance; which one
+ * runs is a performance choice. The pages bound decode by the weight read
+ * (golem, "Qwen3.8 drafts its own next token"), so the kernels differ in how
+ * few instructions they spend per weight byte:
+ *   Q4_DECODE_AUTO       the library's choice for each m (default): the
+ *                        CUDA-core kernel for m <= 2, warp-MMA above;
+ *   Q4_DECODE_WARP_MMA   CUDA cores dequantise to exact fp16 (q - 8), the
+ *                        warp-level MMA (mma.sync) multiplies by X split into
+ *                        fp16 hi + lo, d is applied in fp32 per block;
+ *   Q4_DECODE_CUDA_CORE  exact fp32 (q - 8), fp32 X, fp32 FMAs (m <= 4; wider
+ *                        calls take Q4_DECODE_WARP_MMA);
+ *   Q4_DECODE_TCGEN05    (q - 8) * d rounded to fp16 into tensor memory, X
+ *                        split into fp16 hi + lo, tcgen05.mma.
+ * The setting is kept per process and applies to launches made after the
+ * call. Other values are refused with Q4_ERR_INVALID_ARG. */
+#define Q4_DECODE_AUTO 0
+#define Q4_DECODE_WARP_MMA 1
+#define Q4_DECODE_CUDA_CORE 2
+#define Q4_DECODE_TCGEN05 3
+Q4MM_API int q4_set_decode_kernel(int kind);
 
 /* Profiling builds only (compiled with -DQ4MM_TRACE): kernels launched after
  * the call write 16-byte event records {globaltimer ns, event << 16 | warp

@@ -45,7 +45,7 @@ _SIGS = {
     "q4_last_device_status": (_INT, [_INT]),
     "q4_set_wait_limit_ns": (_INT, [ctypes.c_uint64]),
     "q4_set_weight_prefetch": (_INT, [_INT]),
-    "q4_set_gemv_max_m": (_INT, [_INT]),
+    "q4_set_decode_kernel": (_INT, [_INT]),
     "q4_selftest_wait_timeout": (_INT, [ctypes.c_uint64, _P]),
     "q4_debug_set_trace": (_INT, [_P, _SZ, ctypes.c_uint32]),
 }
@@ -174,8 +174,14 @@ def q4_set_weight_prefetch(enable: bool) -> int:
     return _check(_lib.q4_set_weight_prefetch(1 if enable else 0), "q4_set_weight_prefetch")
 
 
-def q4_set_gemv_max_m(max_m: int) -> int:
-    return _check(_lib.q4_set_gemv_max_m(int(max_m)), "q4_set_gemv_max_m")
+Q4_DECODE_AUTO = 0
+Q4_DECODE_WARP_MMA = 1
+Q4_DECODE_CUDA_CORE = 2
+Q4_DECODE_TCGEN05 = 3
+
+
+def q4_set_decode_kernel(kind: int) -> int:
+    return _check(_lib.q4_set_decode_kernel(int(kind)), "q4_set_decode_kernel")
 
 
 def q4_debug_set_trace(buffer, nbytes: int, cta: int = 0, check: bool = True) -> int:

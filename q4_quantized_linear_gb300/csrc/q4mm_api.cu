@@ -1,7 +1,7 @@
 // q4mm_api.cu -- the C ABI of libq4mm (declared in include/q4mm.h): argument
 // validation, per-device state, workspace handling and dispatch between the
-// CUDA-core GEMV kernel (m <= 2 by default), the tensor-core decode kernel
-// (up to m = 16) and the tensor-core prefill kernels (m > 16).
+// decode kernels (m <= 16: warp-MMA, CUDA-core or tcgen05) and the
+// tensor-core prefill kernels (m > 16).
 //
 // The decode/prefill dispatch point follows golem, "Reading a prompt on the
 // card": the mat-vec is built up to sixteen columns and tiled products take
@@ -28,7 +28,7 @@ constexpr int64_t kDecodeMaxM = 16;
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
 std::atomic<int> g_prefetch_w{0};
-std::atomic<int> g_gemv_max_m{2};
+std::atomic<int> g_decode_kernel{Q4_DECODE_AUTO};
 std::mutex g_trace_mutex;
 TraceSettings g_trace;
 
@@ -177,7 +177,17 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.np = static_cast<int>(ceil_div(k, kPairK));
         a.groups = static_cast<int>(ceil_div(n, kGroupRows));
         a.prefetch_w = g_prefetch_w.load();
-        if (m <= g_gemv_max_m.load()) {
+        int kind = g_decode_kernel.load();
+        // measured on GB300 (graph replays, weights cycled beyond L2): the
+        // CUDA-core kernel is fastest for m <= 2, the warp-MMA kernel from m = 3
+        if (kind == Q4_DECODE_AUTO) kind = m <= 2 ? Q4_DECODE_CUDA_CORE : Q4_DECODE_WARP_MMA;
+        if (kind == Q4_DECODE_CUDA_CORE && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;
+        if (kind == Q4_DECODE_WARP_MMA) {
+            MmvPlan mp;
+            if (!plan_mmv(m, k, n, dev.sm_count, &mp)) return Q4_ERR_INVALID_ARG;
+            return map_cuda(launch_mmv(mp, a, s));
+        }
+        if (kind == Q4_DECODE_CUDA_CORE) {
             GemvPlan gp;
             if (!plan_gemv(m, k, n, dev.sm_count, &gp)) return Q4_ERR_INVALID_ARG;
             return map_cuda(launch_gemv(gp, a, s));
@@ -412,10 +422,10 @@ Q4MM_API int q4_set_weight_prefetch(int enable)
     return Q4_OK;
 }
 
-Q4MM_API int q4_set_gemv_max_m(int max_m)
+Q4MM_API int q4_set_decode_kernel(int kind)
 {
-    if (max_m < 0 || max_m > kGemvMaxM) return Q4_ERR_INVALID_ARG;
-    g_gemv_max_m.store(max_m);
+    if (kind < Q4_DECODE_AUTO || kind > Q4_DECODE_TCGEN05) return Q4_ERR_INVALID_ARG;
+    g_decode_kernel.store(kind);
     return Q4_OK;
 }
 

@@ -147,44 +147,18 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// The same tests, letting the hardware suspend the thread for up to
-// `hint_ns` until the phase completes (a waiting warp then issues nothing).
-__device__ __forceinline__ bool mbar_try_wait_for(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster_for(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Suspension granted per try while waiting (the bound is checked between tries).
-constexpr uint32_t kSuspendHintNs = 100000;
-
 // Wait for the phase of `bar` with parity `parity` to complete, for at most
-// limit_ns nanoseconds. Returns false if the limit ran out.
+// limit_ns nanoseconds. Returns false if the limit ran out. Each try_wait may
+// suspend the thread for a system-dependent time; it resumes when the phase
+// completes (measured on GB300: ~170 ns after a local arrival, ~450 ns after
+// a remote one; a try_wait given a suspend-time hint resumed ~560 ns after a
+// local arrival, so none is given).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait_for(bar, parity, kSuspendHintNs)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -194,7 +168,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait_cluster_for(bar, parity, kSuspendHintNs)) return true;
+        if (mbar_try_wait_cluster(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }

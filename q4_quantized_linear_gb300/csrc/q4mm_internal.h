@@ -116,6 +116,20 @@ struct GemvPlan {
 bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan);
 cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, cudaStream_t s);
 
+// ------------------------------------------------------------ warp MMA --
+
+struct MmvPlan {
+    int NT = 1;            // MMA column tiles: four tokens (hi, lo) each
+    int S = 1;             // K slices = cluster size
+    int clusters = 0;      // persistent clusters: cluster c owns groups c, c + clusters, ...
+    int ctas = 0;          // clusters x S
+    int ring = 8;          // weight-record ring depth
+    size_t smem = 0;
+};
+
+bool plan_mmv(int64_t m, int64_t k, int64_t n, int sm_count, MmvPlan *plan);
+cudaError_t launch_mmv(const MmvPlan &plan, const DecodeArgs &args, cudaStream_t s);
+
 // --------------------------------------------------------------- prefill --
 
 struct PrefillArgs {

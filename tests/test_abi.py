@@ -81,10 +81,9 @@ def test_pack_rejects_bad_arguments_on_the_host(q4lib):
     assert q4lib.q4_0_unpack(0x1001, 0x1000, 64, 64, stream=0, check=False) == 2
 
 
-def test_gemv_threshold_setting_is_checked(q4lib):
-    # 0..4 accepted (host-only setting), anything else refused; default restored
-    for bad in (-1, 5, 16):
-        assert q4lib._lib.q4_set_gemv_max_m(bad) == 1
-    for good in (0, 1, 4):
-        assert q4lib._lib.q4_set_gemv_max_m(good) == 0
-    assert q4lib._lib.q4_set_gemv_max_m(2) == 0
+def test_decode_kernel_setting_is_checked(q4lib):
+    # 0..3 accepted (host-only setting), anything else refused; default restored
+    for bad in (-1, 4, 16):
+        assert q4lib._lib.q4_set_decode_kernel(bad) == 1
+    for good in (1, 2, 3, 0):
+        assert q4lib._lib.q4_set_decode_kernel(good) == 0

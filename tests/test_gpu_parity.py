@@ -45,70 +45,58 @@ def test_pack_matches_oracle_layout_and_unpack_inverts(q4lib, oracle_mod, n, k):
 
 SHAPES = [(1, 32), (64, 64), (65, 96), (200, 1056), (1000, 2080), (333, 4096), (130, 8192 + 64)]
 
+# The decode kernels (m <= 16) selectable through q4_set_decode_kernel.
+DECODE_KERNELS = {"warp_mma": 1, "cuda_core": 2, "tcgen05": 3}
+
+
+@pytest.fixture(params=sorted(DECODE_KERNELS))
+def decode_kernel(request, q4lib):
+    """Run the test once per decode kernel; the library's own choice again after."""
+    q4lib.q4_set_decode_kernel(DECODE_KERNELS[request.param])
+    yield request.param
+    q4lib.q4_set_decode_kernel(q4lib.Q4_DECODE_AUTO)
+
+
+def once_for_prefill(decode_kernel, m):
+    """m > 16 never takes a decode kernel: run such a case under one of them."""
+    if m > 16 and decode_kernel != "warp_mma":
+        pytest.skip("prefill case: decode kernel irrelevant")
+    if decode_kernel == "cuda_core" and m > 4:
+        pytest.skip("the CUDA-core kernel serves m <= 4")
+
 
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8, 9, 13, 16])
 @pytest.mark.parametrize("n,k", SHAPES)
-def test_decode_parity(q4lib, oracle_mod, m, n, k):
+def test_decode_parity(q4lib, oracle_mod, decode_kernel, m, n, k):
+    once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=1000 + n)
     X = synth.activations(m, k, seed=2000 + m)
     W = pack_dev(q4lib, blocks, n, k)
     Y = run_matmul(q4lib, W, X, n)
     Yr, B = oracle_mod.matmul(blocks, X, n, k)
-    assert_parity(Y, Yr, B, m, f"decode m={m} n={n} k={k}")
+    assert_parity(Y, Yr, B, m, f"{decode_kernel} m={m} n={n} k={k}")
 
 
-@pytest.fixture
-def tensor_decode_kernel(q4lib):
-    """Send every m <= 16 to the tensor-core decode kernel for one test."""
-    q4lib.q4_set_gemv_max_m(0)
-    yield
-    q4lib.q4_set_gemv_max_m(2)
-
-
-@pytest.fixture
-def gemv_kernel_to_4(q4lib):
-    """Send every m <= 4 to the CUDA-core GEMV kernel for one test."""
-    q4lib.q4_set_gemv_max_m(4)
-    yield
-    q4lib.q4_set_gemv_max_m(2)
-
-
-@pytest.mark.parametrize("m", [1, 2, 3, 4])
-@pytest.mark.parametrize("n,k", SHAPES)
-def test_tensor_decode_kernel_small_m(q4lib, oracle_mod, tensor_decode_kernel, m, n, k):
-    """The smallest m normally run on the CUDA-core GEMV kernel; the
-    tensor-core decode kernel must meet the same bound there."""
-    blocks = synth.q4_0_blocks(n, k, seed=1000 + n)
-    X = synth.activations(m, k, seed=2000 + m)
-    W = pack_dev(q4lib, blocks, n, k)
-    Y = run_matmul(q4lib, W, X, n)
-    Yr, B = oracle_mod.matmul(blocks, X, n, k)
-    assert_parity(Y, Yr, B, m, f"tensor decode m={m} n={n} k={k}")
-
-
-@pytest.mark.parametrize("m", [1, 2, 3, 4])
-@pytest.mark.parametrize("n,k", SHAPES)
-def test_gemv_kernel_parity(q4lib, oracle_mod, gemv_kernel_to_4, m, n, k):
-    blocks = synth.q4_0_blocks(n, k, seed=1000 + n)
-    X = synth.activations(m, k, seed=2000 + m)
-    W = pack_dev(q4lib, blocks, n, k)
-    Y = run_matmul(q4lib, W, X, n)
-    Yr, B = oracle_mod.matmul(blocks, X, n, k)
-    assert_parity(Y, Yr, B, m, f"gemv m={m} n={n} k={k}")
-
-
-@pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (2, 14336, 4096), (3, 2560, 9728), (4, 151936, 256)])
-def test_gemv_kernel_is_fp32_accurate(q4lib, oracle_mod, gemv_kernel_to_4, m, n, k):
+@pytest.mark.parametrize("kind,m,n,k,rtol", [
+    ("cuda_core", 1, 9728, 2560, 2e-5), ("cuda_core", 2, 14336, 4096, 2e-5),
+    ("cuda_core", 3, 2560, 9728, 2e-5), ("cuda_core", 4, 151936, 256, 2e-5),
+    ("warp_mma", 1, 9728, 2560, 1e-4), ("warp_mma", 4, 2560, 9728, 1e-4),
+    ("warp_mma", 9, 14336, 4096, 1e-4), ("warp_mma", 16, 1000, 2080, 1e-4)])
+def test_decode_kernel_accuracy_margin(q4lib, oracle_mod, kind, m, n, k, rtol):
     """The CUDA-core kernel forms (q - 8) exactly and multiplies fp32 X
-    unrounded: its error is a few fp32 roundings of B, far inside the decode
-    bound (checked at 1/50 of it)."""
+    unrounded; the warp-MMA kernel forms (q - 8) exactly and keeps 22 bits of
+    X per block: both stay far inside the decode bound (checked at rtol)."""
     blocks = synth.q4_0_blocks(n, k, seed=91)
     X = synth.activations(m, k, seed=92)
     W = pack_dev(q4lib, blocks, n, k)
-    Y = run_matmul(q4lib, W, X, n).astype(np.float64)
+    q4lib.q4_set_decode_kernel(DECODE_KERNELS[kind])
+    try:
+        Y = run_matmul(q4lib, W, X, n).astype(np.float64)
+    finally:
+        q4lib.q4_set_decode_kernel(q4lib.Q4_DECODE_AUTO)
     Yr, B = oracle_mod.matmul(blocks, X, n, k)
-    ratio = float((np.abs(Y - Yr) / (2e-5 * B + 1e-7)).max())
-    assert ratio <= 1.0, f"m={m}: max err / (2e-5 B + 1e-7) = {ratio:.3g}"
+    ratio = float((np.abs(Y - Yr) / (rtol * B + 1e-7)).max())
+    assert ratio <= 1.0, f"{kind} m={m}: max err / ({rtol} B + 1e-7) = {ratio:.3g}"
 
 
 @pytest.mark.parametrize("m", [17, 31, 64, 100, 257, 300])
@@ -144,7 +132,8 @@ FULL = [  # (m, n, k): oracle compares every element
 
 
 @pytest.mark.parametrize("m,n,k", FULL)
-def test_workload_sizes_full_compare(q4lib, oracle_mod, m, n, k):
+def test_workload_sizes_full_compare(q4lib, oracle_mod, decode_kernel, m, n, k):
+    once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=0)
     X = synth.activations(m, k, seed=0)
     W = pack_dev(q4lib, blocks, n, k)
@@ -153,8 +142,9 @@ def test_workload_sizes_full_compare(q4lib, oracle_mod, m, n, k):
     assert_parity(Y, Yr, B, m, f"m={m} n={n} k={k}")
 
 
-@pytest.mark.parametrize("m,n,k", [(4, 151936, 2560), (540, 9728, 2560)])
-def test_workload_sizes_sampled(q4lib, oracle_mod, m, n, k):
+@pytest.mark.parametrize("m,n,k", [(4, 151936, 2560), (16, 151936, 2560), (540, 9728, 2560)])
+def test_workload_sizes_sampled(q4lib, oracle_mod, decode_kernel, m, n, k):
+    once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=0)
     X = synth.activations(m, k, seed=0)
     W = pack_dev(q4lib, blocks, n, k)
@@ -174,7 +164,8 @@ def test_workload_sizes_sampled(q4lib, oracle_mod, m, n, k):
 
 @pytest.mark.parametrize("m,slots,n,k", [(1, 8, 300, 512), (4, 40, 9728, 2560), (16, 20, 200, 4096),
                                          (4, 12, 2560, 9728), (20, 64, 260, 1024), (37, 40, 130, 640)])
-def test_batched_slots(q4lib, oracle_mod, m, slots, n, k):
+def test_batched_slots(q4lib, oracle_mod, decode_kernel, m, slots, n, k):
+    once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=11)
     ldx, ldy = k + 8, n + 5
     Xs = np.zeros((slots, ldx), dtype=np.float32)
@@ -211,7 +202,8 @@ def test_m_zero_is_a_no_op(q4lib):
 
 
 @pytest.mark.parametrize("m", [1, 2, 4, 7, 16, 17, 100])
-def test_all_eights_give_exact_zero(q4lib, m):
+def test_all_eights_give_exact_zero(q4lib, decode_kernel, m):
+    once_for_prefill(decode_kernel, m)
     n, k = 130, 640
     blocks = synth.q4_0_blocks(n, k, seed=21)
     blocks[:, :, 2:] = 0x88
@@ -221,9 +213,10 @@ def test_all_eights_give_exact_zero(q4lib, m):
 
 
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 16, 17, 64, 300])
-def test_exact_integer_case_is_bit_exact(q4lib, oracle_mod, m):
+def test_exact_integer_case_is_bit_exact(q4lib, oracle_mod, decode_kernel, m):
     """Power-of-two scales and small integer X: every partial sum is an exact
-    integer times a power of two, on both paths, so the results are equal."""
+    integer times a power of two, on every path, so the results are equal."""
+    once_for_prefill(decode_kernel, m)
     n, k = 200, 1024
     blocks = synth.q4_0_blocks(n, k, seed=31)
     nb = k // 32
@@ -238,7 +231,8 @@ def test_exact_integer_case_is_bit_exact(q4lib, oracle_mod, m):
 
 
 @pytest.mark.parametrize("m", [1, 3, 5, 16, 17, 64])
-def test_nonfinite_x_propagates(q4lib, oracle_mod, m):
+def test_nonfinite_x_propagates(q4lib, oracle_mod, decode_kernel, m):
+    once_for_prefill(decode_kernel, m)
     n, k = 100, 256
     blocks = synth.q4_0_blocks(n, k, seed=41)
     X = synth.activations(m, k, seed=42)
@@ -251,7 +245,8 @@ def test_nonfinite_x_propagates(q4lib, oracle_mod, m):
 
 
 @pytest.mark.parametrize("m", [3, 6, 33])
-def test_zero_and_negative_scales(q4lib, oracle_mod, m):
+def test_zero_and_negative_scales(q4lib, oracle_mod, decode_kernel, m):
+    once_for_prefill(decode_kernel, m)
     n, k = 96, 512
     blocks = synth.q4_0_blocks(n, k, seed=51)
     blocks[::3, ::2, 0:2] = 0                       # d = +0
@@ -264,7 +259,8 @@ def test_zero_and_negative_scales(q4lib, oracle_mod, m):
 
 @pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (2, 2560, 9728), (4, 2560, 9728), (8, 2560, 9728),
                                    (16, 14336, 4096), (540, 9728, 2560)])
-def test_bitwise_deterministic(q4lib, m, n, k):
+def test_bitwise_deterministic(q4lib, decode_kernel, m, n, k):
+    once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=61)
     X = synth.activations(m, k, seed=62)
     W = pack_dev(q4lib, blocks, n, k)
@@ -275,8 +271,9 @@ def test_bitwise_deterministic(q4lib, m, n, k):
 
 @pytest.mark.parametrize("m,n,k", [(1, 9728, 2560), (4, 2560, 9728), (8, 2560, 9728), (16, 1000, 2080),
                                    (100, 1000, 2080)])
-def test_weight_prefetch_mode_gives_identical_results(q4lib, oracle_mod, m, n, k):
+def test_weight_prefetch_mode_gives_identical_results(q4lib, oracle_mod, decode_kernel, m, n, k):
     """Streaming W before the preceding kernel finishes changes timing only."""
+    once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=81)
     X = synth.activations(m, k, seed=82)
     W = pack_dev(q4lib, blocks, n, k)
