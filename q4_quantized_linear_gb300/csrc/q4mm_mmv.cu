@@ -40,7 +40,7 @@
 //     that order) through a ring of R shared-memory slots with 1-D bulk
 //     copies;
 //   * warps 0-7: first stage the CTA's slice of X as B fragments in shared
-//     memory (after the dependency wait), then warp c takes rows 16c .. 16c +
+//     memory (after the dependency wait), then warp w takes rows 16w .. 16w +
 //     15 of every record: no partial sums cross warps, and each warp holds
 //     its rows' totals in registers until the group ends.
 // Every wait is bounded and warp-uniform; a slot's full barrier is waited on
@@ -61,8 +61,7 @@ namespace q4 {
 namespace {
 
 constexpr int kErrTimeout = 5;      // Q4_ERR_DEVICE_TIMEOUT
-constexpr int kRT = 1;              // 16-row MMA tiles a consumer warp owns in every record
-constexpr int kCWarps = kGroupRows / (16 * kRT);   // consumer warps
+constexpr int kCWarps = 8;          // consumer warps
 constexpr int kThreads = (kCWarps + 1) * 32;
 constexpr int kMaxSlices = 8;
 constexpr int kMaxRing = 32;
@@ -74,7 +73,7 @@ struct MSmem {
     float *xsc;          // [P][2][16] 2^-e of (pair, block, token)
     float *part;         // [2][16][128] this CTA's row totals of a group (S > 1)
     uint64_t *full, *empty;          // [R]
-    uint64_t *red_full, *red_free;   // [2][kCWarps] a row tile's other slices landed / slot free
+    uint64_t *red_full, *red_free;   // [2][8] a row tile's other slices landed / slot free
 };
 
 __device__ __forceinline__ void fail(const DecodeArgs &a) { record_status(a.status, kErrTimeout); }
@@ -123,18 +122,17 @@ __device__ __forceinline__ unsigned absmax_bits(const float4 &v)
                max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu));
 }
 
-// fp16 bits of the hi (h = 0) or lo (h = 1) term of an already scaled value.
-__device__ __forceinline__ uint32_t split_term(float xs, int h)
+// The hi (h = 0) or lo (h = 1) fp16 terms of two already scaled values, as
+// one packed register (x0 in the low half): hi = fp16(x), lo = fp16(x - hi).
+// A block whose largest |x| is not finite gets lo = 0 (its rows' results are
+// infinite or NaN whatever lo holds).
+__device__ __forceinline__ uint32_t split_pair(float x0, float x1, int h, bool finite)
 {
-    const __half hi = __float2half_rn(xs);
-    if (h == 0) return __half_as_ushort(hi);
-    const float r = xs - __half2float(hi);
-    return isfinite(r) ? __half_as_ushort(__float2half_rn(r)) : 0u;
-}
-
-__device__ __forceinline__ uint32_t pack_terms(float x0, float x1, int h)
-{
-    return split_term(x0, h) | (split_term(x1, h) << 16);
+    const __half2 hi = __floats2half2_rn(x0, x1);
+    if (h == 0) return *reinterpret_cast<const uint32_t *>(&hi);
+    const float2 back = __half22float2(hi);
+    const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
+    return finite ? *reinterpret_cast<const uint32_t *>(&lo) : 0u;
 }
 
 // Stage the CTA's slice of X (pairs p0 .. p0 + P - 1) as MMA B fragments.
@@ -148,7 +146,7 @@ template <int NT>
 __device__ __forceinline__ void stage_x(const DecodeArgs &a, const MSmem &sm, int p0, int P, int c, int lane,
                                         const int yrow[kMaxTokens])
 {
-    constexpr int kBatch = 4;                      // entries whose loads are in flight together
+    constexpr int kBatch = 8;                      // entries whose loads are in flight together
     const int g = lane >> 2, t = lane & 3;
     const int h = g & 1;
     const int E = P * 2 * NT;
@@ -185,11 +183,12 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const MSmem &sm, in
                 ex = max(-100, min(100, ex));
             }
             const float su = __uint_as_float(static_cast<unsigned>(ex + 127) << 23);
+            const bool fin = mb < 0x7F800000u;
             uint4 f;
-            f.x = pack_terms(xa[q].x * su, xa[q].z * su, h);
-            f.y = pack_terms(xb[q].x * su, xb[q].z * su, h);
-            f.z = pack_terms(xa[q].y * su, xa[q].w * su, h);
-            f.w = pack_terms(xb[q].y * su, xb[q].w * su, h);
+            f.x = split_pair(xa[q].x * su, xa[q].z * su, h, fin);
+            f.y = split_pair(xb[q].x * su, xb[q].z * su, h, fin);
+            f.z = split_pair(xa[q].y * su, xa[q].w * su, h, fin);
+            f.w = split_pair(xb[q].y * su, xb[q].w * su, h, fin);
             sm.ximg[e * 32 + lane] = f;
             if (h == 0 && t == 0)
                 sm.xsc[pb * kMaxTokens + j] = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);
@@ -269,23 +268,22 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const DecodeArgs a)
         __syncwarp();
     } else {
         // --------------------------------------------------------- consumers
-        // Warp c owns rows 32c .. 32c + 31 of every record: tile r holds rows
-        // 32c + 16r + g (MMA rows g) and 32c + 16r + g + 8 (rows g + 8).
-        const int c = warp;
+        // Warp w: rows 16w + g and 16w + g + 8 of every record (MMA rows g
+        // and g + 8).
+        const int w = warp;
         const int g = lane >> 2, t = lane & 3;
-        const int rbase = 16 * kRT * c + g;
+        const int R0 = 16 * w + g;
         pdl_wait();                                   // X, Y and the slot rows are the preceding kernel's
         int yrow[kMaxTokens];
 #pragma unroll
         for (int j = 0; j < kMaxTokens; ++j) yrow[j] = j < a.m ? (a.rows ? __ldg(a.rows + j) : j) : 0;
-        stage_x<NT>(a, sm, p0, P, c, lane, yrow);
+        stage_x<NT>(a, sm, p0, P, warp, lane, yrow);
         consumers_sync();
 
-        // this thread's byte offsets inside a record
-        const uint32_t off_sc = static_cast<uint32_t>(kRecScaleOff + 4 * rbase);
-        const uint32_t off_q0 = static_cast<uint32_t>(kRecQs0Off + 16 * rbase + 4 * t);
-        const uint32_t off_q1 = static_cast<uint32_t>(kRecQs1Off + 16 * rbase + 4 * t);
         const uint32_t w0 = smem_u32(sm.w);
+        const uint32_t off_sc = static_cast<uint32_t>(kRecScaleOff + 4 * R0);
+        const uint32_t off_q0 = static_cast<uint32_t>(kRecQs0Off + 16 * R0 + 4 * t);
+        const uint32_t off_q1 = static_cast<uint32_t>(kRecQs1Off + 16 * R0 + 4 * t);
         const uint32_t xi0 = smem_u32(sm.ximg) + static_cast<uint32_t>(lane * 16);
         const uint32_t xs0 = smem_u32(sm.xsc) + static_cast<uint32_t>(t * 4);
         const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -293,44 +291,29 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const DecodeArgs a)
         int s = 0;
         uint32_t ph = 0;
         for (int gi = 0; gi < ntiles && ok; ++gi) {
-            float y[NT][kRT][2];
+            float y[NT][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int r = 0; r < kRT; ++r) y[nt][r][0] = y[nt][r][1] = 0.f;
-            uint32_t xi = xi0, xs = xs0;              // X entries of pair j: [2 j + b][nt]
+            for (int nt = 0; nt < NT; ++nt) y[nt][0] = y[nt][1] = 0.f;
             for (int j = 0; j < P; ++j) {
                 if (!warp_wait(&sm.full[s], ph, a.wait_ns)) { ok = false; break; }
                 const uint32_t rec = w0 + static_cast<uint32_t>(s * kRecordBytes);
-                uint32_t sc[kRT][2], q[2][kRT][2];
-#pragma unroll
-                for (int r = 0; r < kRT; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t ro = static_cast<uint32_t>(16 * r + 8 * h);
-                        sc[r][h] = lds32(rec + off_sc + 4 * ro);
-                        q[0][r][h] = lds32(rec + off_q0 + 16 * ro);
-                        q[1][r][h] = lds32(rec + off_q1 + 16 * ro);
-                    }
-                // A fragments [tile][block][k-step]: (q - 8) of rows g, g + 8, exact
-                uint32_t A[kRT][2][2][4];
-#pragma unroll
-                for (int r = 0; r < kRT; ++r)
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        uint32_t v0[4], v1[4];
-                        unpack_word_f16(q[b][r][0], v0);
-                        unpack_word_f16(q[b][r][1], v1);
-                        A[r][b][0][0] = v0[0], A[r][b][0][1] = v1[0], A[r][b][0][2] = v0[1], A[r][b][0][3] = v1[1];
-                        A[r][b][1][0] = v0[2], A[r][b][1][1] = v1[2], A[r][b][1][2] = v0[3], A[r][b][1][3] = v1[3];
-                    }
+                const uint32_t sc0 = lds32(rec + off_sc), sc1 = lds32(rec + off_sc + 32);
+                const uint32_t q00 = lds32(rec + off_q0), q01 = lds32(rec + off_q0 + 128);
+                const uint32_t q10 = lds32(rec + off_q1), q11 = lds32(rec + off_q1 + 128);
+                // A fragments [block][k-step]: (q - 8) of rows g, g + 8, exact
+                uint32_t v00[4], v01[4], v10[4], v11[4];
+                unpack_word_f16(q00, v00);
+                unpack_word_f16(q01, v01);
+                unpack_word_f16(q10, v10);
+                unpack_word_f16(q11, v11);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.empty[s]);   // the warp's share of the slot has been read
-                float2 d[kRT][2];                     // [tile][row g / g + 8] = (block 0, block 1)
-#pragma unroll
-                for (int r = 0; r < kRT; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) d[r][h] = __half22float2(*reinterpret_cast<const __half2 *>(&sc[r][h]));
+                const uint32_t A[2][2][4] = {{{v00[0], v01[0], v00[1], v01[1]}, {v00[2], v01[2], v00[3], v01[3]}},
+                                             {{v10[0], v11[0], v10[1], v11[1]}, {v10[2], v11[2], v10[3], v11[3]}}};
+                const float2 d0 = __half22float2(*reinterpret_cast<const __half2 *>(&sc0));   // row g: block 0, 1
+                const float2 d1 = __half22float2(*reinterpret_cast<const __half2 *>(&sc1));   // row g + 8
+                const uint32_t xi = xi0 + static_cast<uint32_t>(j * 2 * NT * 512);
+                const uint32_t xs = xs0 + static_cast<uint32_t>(j * 2 * kMaxTokens * 4);
 #pragma unroll
                 for (int b = 0; b < 2; ++b) {
 #pragma unroll
@@ -343,75 +326,60 @@ __global__ void __launch_bounds__(kThreads, 2) mmv_kernel(const DecodeArgs a)
                         asm volatile("ld.shared.f32 %0, [%1];"
                                      : "=f"(su)
                                      : "r"(xs + static_cast<uint32_t>((b * kMaxTokens + 4 * nt) * 4)));
-#pragma unroll
-                        for (int r = 0; r < kRT; ++r) {
-                            float D[4];
-                            mma_f16(D, A[r][b][0], bf.x, bf.y, zero4);
-                            mma_f16(D, A[r][b][1], bf.z, bf.w, D);
-                            const float d0 = b ? d[r][0].y : d[r][0].x, d1 = b ? d[r][1].y : d[r][1].x;
-                            y[nt][r][0] = fmaf(d0 * su, D[0] + D[1], y[nt][r][0]);
-                            y[nt][r][1] = fmaf(d1 * su, D[2] + D[3], y[nt][r][1]);
-                        }
+                        float D[4];
+                        mma_f16(D, A[b][0], bf.x, bf.y, zero4);
+                        mma_f16(D, A[b][1], bf.z, bf.w, D);
+                        y[nt][0] = fmaf((b ? d0.y : d0.x) * su, D[0] + D[1], y[nt][0]);
+                        y[nt][1] = fmaf((b ? d1.y : d1.x) * su, D[2] + D[3], y[nt][1]);
                     }
                 }
-                xi += static_cast<uint32_t>(2 * NT * 512);
-                xs += static_cast<uint32_t>(2 * kMaxTokens * 4);
                 if (++s == R) s = 0, ph ^= 1u;
             }
             if (!ok) break;
             // ------------------------------------------------ group gi done
             const int tb = gi & 1;
             const uint32_t par = static_cast<uint32_t>((gi >> 1) & 1);
-            const int64_t gbase = static_cast<int64_t>(G0 + gi * a.clusters) * kGroupRows;
             if (rank > 0) {
                 // rows into this CTA's part[tb]; the first CTA reads them
-                if (gi >= 2 && !warp_wait_cluster(&sm.red_free[tb * kCWarps + c], par ^ 1u, a.wait_ns)) {
+                if (gi >= 2 && !warp_wait_cluster(&sm.red_free[tb * kCWarps + w], par ^ 1u, a.wait_ns)) {
                     ok = false;
                     break;
                 }
                 float *pp = sm.part + tb * kMaxTokens * kGroupRows;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int r = 0; r < kRT; ++r) {
-                        const int tok = 4 * nt + t;
-                        pp[tok * kGroupRows + rbase + 16 * r] = y[nt][r][0];
-                        pp[tok * kGroupRows + rbase + 16 * r + 8] = y[nt][r][1];
-                    }
+                for (int nt = 0; nt < NT; ++nt) {
+                    pp[(4 * nt + t) * kGroupRows + R0] = y[nt][0];
+                    pp[(4 * nt + t) * kGroupRows + R0 + 8] = y[nt][1];
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_full[tb * kCWarps + c]), 0u));
+                if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_full[tb * kCWarps + w]), 0u));
                 continue;
             }
             if (S > 1) {
-                if (!warp_wait_cluster(&sm.red_full[tb * kCWarps + c], par, a.wait_ns)) { ok = false; break; }
+                if (!warp_wait_cluster(&sm.red_full[tb * kCWarps + w], par, a.wait_ns)) { ok = false; break; }
                 const uint32_t pbase = smem_u32(sm.part + tb * kMaxTokens * kGroupRows);
                 for (int rr = 1; rr < S; ++rr) {
                     const uint32_t rp = mapa_shared(pbase, static_cast<uint32_t>(rr));
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int r = 0; r < kRT; ++r) {
-                            const int tok = 4 * nt + t;
-                            const uint32_t o = static_cast<uint32_t>((tok * kGroupRows + rbase + 16 * r) * 4);
-                            y[nt][r][0] += ld_cluster_f32(rp + o);
-                            y[nt][r][1] += ld_cluster_f32(rp + o + 32);
-                        }
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint32_t o = static_cast<uint32_t>(((4 * nt + t) * kGroupRows + R0) * 4);
+                        y[nt][0] += ld_cluster_f32(rp + o);
+                        y[nt][1] += ld_cluster_f32(rp + o + 32);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
                     for (int rr = 1; rr < S; ++rr)
-                        mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_free[tb * kCWarps + c]), static_cast<uint32_t>(rr)));
+                        mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_free[tb * kCWarps + w]), static_cast<uint32_t>(rr)));
             }
+            const int64_t row0 = static_cast<int64_t>(G0 + gi * a.clusters) * kGroupRows + R0;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int tok = 4 * nt + t;
                 if (tok < a.m) {
-                    float *yr = a.Y + static_cast<int64_t>(yrow[tok]) * a.ldy + gbase + rbase;
-#pragma unroll
-                    for (int r = 0; r < kRT; ++r) {
-                        if (gbase + rbase + 16 * r < a.n) yr[16 * r] = y[nt][r][0];
-                        if (gbase + rbase + 16 * r + 8 < a.n) yr[16 * r + 8] = y[nt][r][1];
-                    }
+                    float *yr = a.Y + static_cast<int64_t>(yrow[tok]) * a.ldy + row0;
+                    if (row0 < a.n) yr[0] = y[nt][0];
+                    if (row0 + 8 < a.n) yr[8] = y[nt][1];
                 }
             }
         }
@@ -487,9 +455,10 @@ int mmv_max_clusters(int NT, int S, size_t smem)
 // that fits one CTA's shared memory, and the deepest that leaves room for a
 // second CTA on the SM (the next call's, or this call's). The number of
 // clusters is capped by what the device holds at once (a second wave would
-// double the time). Cost, in record times of one SM's share of HBM: the
-// busiest SM's records at the rate its CTAs sustain, plus per-group and
-// per-slice overheads, plus the start-up that cannot overlap the preceding
+// double the time). Cost, in record times of one SM's share of HBM (about
+// 0.1 us on GB300): the busiest SM's records at the rate its CTAs sustain,
+// plus the cross-CTA reduction of split K (measured about 1.3 us a call),
+// per-group overheads, and the start-up that cannot overlap the preceding
 // call when no SM has room left for the next call's CTA.
 bool plan_mmv(int64_t m, int64_t k, int64_t n, int sm_count, MmvPlan *plan)
 {
@@ -518,10 +487,15 @@ bool plan_mmv(int64_t m, int64_t k, int64_t n, int sm_count, MmvPlan *plan)
             const int64_t tiles = ceil_div(groups, clusters);
             const int64_t ctas = clusters * S;
             const int per_sm = ctas > sm_count ? 2 : 1;
-            const double rate = per_sm == 2 ? 1.0 : (two_fit ? 0.9 : 0.8);
-            const double stream = std::max(static_cast<double>(tiles * P * per_sm) / rate, total / sm_count);
+            // records an SM turns over per record time: one CTA of this kernel
+            // alone on an SM takes about 2.5 record times per record (issue-
+            // bound); two CTAs of the call share an SM at about 0.6 records
+            // per record time (measured on GB300)
+            const double rate = per_sm == 2 ? 0.6 : 0.4;
+            const double recs = static_cast<double>(tiles * P);   // records per CTA
+            const double stream = std::max(recs * per_sm / rate, total / sm_count);
             const double no_overlap = (!two_fit || per_sm == 2) ? 15.0 : 0.0;
-            const double cost = stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 2.0 : 0.0) + no_overlap;
+            const double cost = stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 12.0 : 0.0) + no_overlap;
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.NT = NT;
