@@ -76,9 +76,9 @@ def decode_kernel_name(m):
     """The kernel the library's automatic dispatch runs for m token rows."""
     if m > 16:
         return "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)"
-    if m <= 2:
-        return "gemv_kernel (q4mm_gemv.cu, CUDA cores)"
-    return "mmv_kernel (q4mm_mmv.cu, warp-level MMA)"
+    if m <= 4:
+        return "gemv_kernel<m, true> (q4mm_gemv.cu, whole records per warp on the warp-level MMA)"
+    return "mmv_kernel (q4mm_mmv.cu, row-tiled warp-level MMA)"
 
 
 def load_peaks():

@@ -220,21 +220,26 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
  * runs is a performance choice. The pages bound decode by the weight read
  * (golem, "Qwen3.8 drafts its own next token"), so the kernels differ in how
  * few instructions they spend per weight byte:
- *   Q4_DECODE_AUTO       the library's choice for each m (default): the
- *                        CUDA-core kernel for m <= 2, warp-MMA above;
+ *   Q4_DECODE_AUTO       the library's choice for each m (default): record
+ *                        MMA for m <= 4, warp-MMA above;
  *   Q4_DECODE_WARP_MMA   CUDA cores dequantise to exact fp16 (q - 8), the
  *                        warp-level MMA (mma.sync) multiplies by X split into
  *                        fp16 hi + lo, d is applied in fp32 per block;
  *   Q4_DECODE_CUDA_CORE  exact fp32 (q - 8), fp32 X, fp32 FMAs (m <= 4; wider
  *                        calls take Q4_DECODE_WARP_MMA);
  *   Q4_DECODE_TCGEN05    (q - 8) * d rounded to fp16 into tensor memory, X
- *                        split into fp16 hi + lo, tcgen05.mma.
+ *                        split into fp16 hi + lo, tcgen05.mma;
+ *   Q4_DECODE_RECORD_MMA each warp takes whole records: exact fp16 (q - 8)
+ *                        times X split per block into fp16 hi + lo on the
+ *                        warp-level MMA, d applied in fp32 per block (m <= 4;
+ *                        wider calls take Q4_DECODE_WARP_MMA).
  * The setting is kept per process and applies to launches made after the
  * call. Other values are refused with Q4_ERR_INVALID_ARG. */
 #define Q4_DECODE_AUTO 0
 #define Q4_DECODE_WARP_MMA 1
 #define Q4_DECODE_CUDA_CORE 2
 #define Q4_DECODE_TCGEN05 3
+#define Q4_DECODE_RECORD_MMA 4
 Q4MM_API int q4_set_decode_kernel(int kind);
 
 /* Profiling builds only (compiled with -DQ4MM_TRACE): kernels launched after

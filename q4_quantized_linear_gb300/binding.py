@@ -178,6 +178,7 @@ Q4_DECODE_AUTO = 0
 Q4_DECODE_WARP_MMA = 1
 Q4_DECODE_CUDA_CORE = 2
 Q4_DECODE_TCGEN05 = 3
+Q4_DECODE_RECORD_MMA = 4
 
 
 def q4_set_decode_kernel(kind: int) -> int:

@@ -178,19 +178,20 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.groups = static_cast<int>(ceil_div(n, kGroupRows));
         a.prefetch_w = g_prefetch_w.load();
         int kind = g_decode_kernel.load();
-        // measured on GB300 (graph replays, weights cycled beyond L2): the
-        // CUDA-core kernel is fastest for m <= 2, the warp-MMA kernel from m = 3
-        if (kind == Q4_DECODE_AUTO) kind = m <= 2 ? Q4_DECODE_CUDA_CORE : Q4_DECODE_WARP_MMA;
-        if (kind == Q4_DECODE_CUDA_CORE && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;
+        // measured on GB300 (graph replays, weights cycled beyond L2): whole
+        // records per warp on the warp-level MMA are fastest for m <= 4 on
+        // every layer measured, the row-tiled warp-MMA kernel above
+        if (kind == Q4_DECODE_AUTO) kind = m <= kGemvMaxM ? Q4_DECODE_RECORD_MMA : Q4_DECODE_WARP_MMA;
+        if ((kind == Q4_DECODE_CUDA_CORE || kind == Q4_DECODE_RECORD_MMA) && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;
         if (kind == Q4_DECODE_WARP_MMA) {
             MmvPlan mp;
             if (!plan_mmv(m, k, n, dev.sm_count, &mp)) return Q4_ERR_INVALID_ARG;
             return map_cuda(launch_mmv(mp, a, s));
         }
-        if (kind == Q4_DECODE_CUDA_CORE) {
+        if (kind == Q4_DECODE_CUDA_CORE || kind == Q4_DECODE_RECORD_MMA) {
             GemvPlan gp;
             if (!plan_gemv(m, k, n, dev.sm_count, &gp)) return Q4_ERR_INVALID_ARG;
-            return map_cuda(launch_gemv(gp, a, s));
+            return map_cuda(launch_gemv(gp, a, kind == Q4_DECODE_RECORD_MMA, s));
         }
         DecodePlan plan;
         if (!plan_decode(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
@@ -424,7 +425,7 @@ Q4MM_API int q4_set_weight_prefetch(int enable)
 
 Q4MM_API int q4_set_decode_kernel(int kind)
 {
-    if (kind < Q4_DECODE_AUTO || kind > Q4_DECODE_TCGEN05) return Q4_ERR_INVALID_ARG;
+    if (kind < Q4_DECODE_AUTO || kind > Q4_DECODE_RECORD_MMA) return Q4_ERR_INVALID_ARG;
     g_decode_kernel.store(kind);
     return Q4_OK;
 }

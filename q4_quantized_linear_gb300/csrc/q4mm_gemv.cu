@@ -203,6 +203,123 @@ __device__ __forceinline__ void gemv_block(const uint8_t *qs, uint32_t dsh, cons
     }
 }
 
+// ------------------------------------------------------------------------
+// Record-MMA mode (m <= 4): the same warps, ring and reductions, but a warp
+// turns its record's nibbles into exact fp16 (q - 8) (lop3 magic and one fp16
+// FMA per two weights) and multiplies them by X on the tensor core with
+// mma.sync m16n8k16, 16 rows at a time. The MMA's K index is a permutation of
+// a block's elements chosen so that thread (g, t) of the warp (lane 4g + t)
+// takes its A registers straight from word t of its rows' 16 nibble bytes;
+// X's B fragments use the same permutation. Column g of the 8 is token g / 2,
+// its hi (g even) or lo (g odd) fp16 term after the block is scaled by a power
+// of two (largest |x| into [2^14, 2^15)): 22 significant bits relative to the
+// block's largest |x|. d is applied in fp32 per block.
+
+__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1, const float c[4])
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+                   "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ unsigned absmax_bits(const float4 &v)
+{
+    return max(max(__float_as_uint(v.x) & 0x7FFFFFFFu, __float_as_uint(v.y) & 0x7FFFFFFFu),
+               max(__float_as_uint(v.z) & 0x7FFFFFFFu, __float_as_uint(v.w) & 0x7FFFFFFFu));
+}
+
+// The hi (h = 0) or lo (h = 1) fp16 terms of two scaled values, packed (x0 in
+// the low half). A block whose largest |x| is not finite gets lo = 0 (its
+// rows' results are infinite or NaN whatever lo holds).
+__device__ __forceinline__ uint32_t split_pair(float x0, float x1, int h, bool finite)
+{
+    const __half2 hi = __floats2half2_rn(x0, x1);
+    if (h == 0) return *reinterpret_cast<const uint32_t *>(&hi);
+    const float2 back = __half22float2(hi);
+    const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
+    return finite ? *reinterpret_cast<const uint32_t *>(&lo) : 0u;
+}
+
+// This lane's 8 X values of block blk for its column's token (token g / 2):
+// elements 4t .. 4t + 3 and 16 + 4t .. 19 + 4t; lanes 4g .. 4g + 3 together
+// hold the block. Zero when the column or the block is not live.
+__device__ __forceinline__ void x_load(const float *xrow, int blk, bool live, int lane, float4 &xa, float4 &xb)
+{
+    const int t = lane & 3;
+    xa = make_float4(0.f, 0.f, 0.f, 0.f);
+    xb = xa;
+    if (live) {
+        const float *xr = xrow + 32 * blk + 4 * t;
+        xa = __ldg(reinterpret_cast<const float4 *>(xr));
+        xb = __ldg(reinterpret_cast<const float4 *>(xr + 16));
+    }
+}
+
+// B fragments of one block from this lane's X values (column g: token g / 2,
+// term g % 2), and the inverse scale of the token this lane's accumulators
+// hold (t).
+__device__ __forceinline__ void x_fragments(const float4 &xa, const float4 &xb, int lane, uint4 &bf, float &su_t)
+{
+    const int g = lane >> 2, t = lane & 3, h = g & 1;
+    unsigned mb = max(absmax_bits(xa), absmax_bits(xb));
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+    int ex = 0;
+    if (mb != 0 && mb < 0x7F800000u) {
+        const int E2 = static_cast<int>(mb >> 23) - 126;   // |x|max = f 2^E2, f in [0.5, 1) (normal)
+        ex = (mb >> 23) == 0 ? 100 : 15 - E2;
+        ex = max(-100, min(100, ex));
+    }
+    const float su = __uint_as_float(static_cast<unsigned>(ex + 127) << 23);
+    const bool fin = mb < 0x7F800000u;
+    bf.x = split_pair(xa.x * su, xa.z * su, h, fin);   // k-step 0: elements 4t, 4t+2
+    bf.y = split_pair(xb.x * su, xb.z * su, h, fin);   //           16+4t, 18+4t
+    bf.z = split_pair(xa.y * su, xa.w * su, h, fin);   // k-step 1: 4t+1, 4t+3
+    bf.w = split_pair(xb.y * su, xb.w * su, h, fin);   //           17+4t, 19+4t
+    const float inv = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);
+    su_t = __shfl_sync(0xFFFFFFFFu, inv, 8 * t);       // column 2t: token t's hi term
+}
+
+// One record through the tensor core: y[rt][0 / 1] += rows 16 rt + g and
+// 16 rt + g + 8, token t (lane 4g + t).
+__device__ __forceinline__ void mma_record(const uint8_t *rec, const uint4 bf[2], const float su[2], int lane,
+                                           float y[8][2])
+{
+    const int g = lane >> 2, t = lane & 3;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t base = smem_u32(rec);
+#pragma unroll
+    for (int rt = 0; rt < 8; ++rt) {
+        const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
+        uint32_t sc0, sc1, q00, q01, q10, q11;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc0) : "r"(base + kRecScaleOff + 4 * r0));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc1) : "r"(base + kRecScaleOff + 4 * r0 + 32));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q00) : "r"(base + kRecQs0Off + 16 * r0 + 4 * t));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q01) : "r"(base + kRecQs0Off + 16 * r0 + 4 * t + 128));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q10) : "r"(base + kRecQs1Off + 16 * r0 + 4 * t));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q11) : "r"(base + kRecQs1Off + 16 * r0 + 4 * t + 128));
+        uint32_t v00[4], v01[4], v10[4], v11[4];
+        unpack_word_f16(q00, v00);
+        unpack_word_f16(q01, v01);
+        unpack_word_f16(q10, v10);
+        unpack_word_f16(q11, v11);
+        const uint32_t A[2][2][4] = {{{v00[0], v01[0], v00[1], v01[1]}, {v00[2], v01[2], v00[3], v01[3]}},
+                                     {{v10[0], v11[0], v10[1], v11[1]}, {v10[2], v11[2], v10[3], v11[3]}}};
+        const float2 d0 = __half22float2(*reinterpret_cast<const __half2 *>(&sc0));   // row g: block 0, 1
+        const float2 d1 = __half22float2(*reinterpret_cast<const __half2 *>(&sc1));   // row g + 8
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            float D[4];
+            mma_f16(D, A[b][0], bf[b].x, bf[b].y, zero4);
+            mma_f16(D, A[b][1], bf[b].z, bf[b].w, D);
+            y[rt][0] = fmaf((b ? d0.y : d0.x) * su[b], D[0] + D[1], y[rt][0]);
+            y[rt][1] = fmaf((b ? d1.y : d1.x) * su[b], D[2] + D[3], y[rt][1]);
+        }
+    }
+}
+
 // Issue the bulk copy of the CTA's record (group i of its cluster, pair j of
 // its slice) into ring slot s. Lane 0 of the slot's warp only.
 __device__ __forceinline__ void load_record(const DecodeArgs &a, const GSmem &sm, int i, int j, int s, int G0,
@@ -283,7 +400,7 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &s
     return true;
 }
 
-template <int M>
+template <int M, bool MMA>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -350,11 +467,23 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         yrow[t] = t < a.m ? (a.rows ? __ldg(a.rows + t) : t) : 0;
         xr[t] = a.X + static_cast<int64_t>(yrow[t]) * a.ldx;
     }
+    // record-MMA mode: this lane's B column is token (lane / 8)
+    const int col_tok = lane >> 3;
+    const bool col_live = col_tok < M && col_tok < a.m;
+    const float *xcol = a.X + (col_live ? static_cast<int64_t>(a.rows ? __ldg(a.rows + col_tok) : col_tok) * a.ldx : 0);
 
     bool ok = true;
     int s = c;
     uint32_t ph = 0;
     int pending = c;                                  // first of this warp's records not yet read
+    // record-MMA mode: X values of the warp's next record, loaded one record
+    // ahead so that their latency hides behind the current record's work
+    float4 xn[2][2];
+    if (MMA && ci < ntiles) {
+        const int b0 = 2 * (p0 + cj);
+        x_load(xcol, b0, col_live, lane, xn[0][0], xn[0][1]);
+        x_load(xcol, b0 + 1, col_live && b0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
+    }
     for (int g = 0; g < ntiles && ok; ++g) {
         const int tb = g & 1;
         float yp[4][M];
@@ -362,15 +491,34 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int t = 0; t < M; ++t) yp[r][t] = 0.0f;
+        float yq[8][2];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) yq[r][0] = yq[r][1] = 0.0f;
         for (; ci == g; step_pos(ci, cj, P)) {
             if (!warp_wait(&sm.full_w[s], ph, a.wait_ns)) { ok = false; break; }
             const uint8_t *rec = sm.w + static_cast<size_t>(s) * kRecordBytes;
-            uint32_t sc[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) sc[r] = lds32(rec + kRecScaleOff + 4 * (lane + 32 * r));
             const int b0 = 2 * (p0 + cj);
-            gemv_block<M>(rec + kRecQs0Off, 0, sc, xr, 32 * b0, lane, kc, yp);
-            if (b0 + 1 < a.nb) gemv_block<M>(rec + kRecQs1Off, 16, sc, xr, 32 * (b0 + 1), lane, kc, yp);
+            if (MMA) {
+                // a missing second block is padding (weights exactly 0) against X = 0
+                uint4 bf[2];
+                float su[2];
+                x_fragments(xn[0][0], xn[0][1], lane, bf[0], su[0]);
+                x_fragments(xn[1][0], xn[1][1], lane, bf[1], su[1]);
+                int ni = ci, nj = cj;
+                step_pos(ni, nj, P);
+                if (ni < ntiles) {
+                    const int nb0 = 2 * (p0 + nj);
+                    x_load(xcol, nb0, col_live, lane, xn[0][0], xn[0][1]);
+                    x_load(xcol, nb0 + 1, col_live && nb0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
+                }
+                mma_record(rec, bf, su, lane, yq);
+            } else {
+                uint32_t sc[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) sc[r] = lds32(rec + kRecScaleOff + 4 * (lane + 32 * r));
+                gemv_block<M>(rec + kRecQs0Off, 0, sc, xr, 32 * b0, lane, kc, yp);
+                if (b0 + 1 < a.nb) gemv_block<M>(rec + kRecQs1Off, 16, sc, xr, 32 * (b0 + 1), lane, kc, yp);
+            }
             // Every lane has its values of the slot in registers: refill it
             // with the record R places ahead (same warp, same slot).
             __syncwarp();
@@ -383,10 +531,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         if (!ok) break;
         if (g >= 2 && !warp_wait(&sm.gfree[tb], ((g >> 1) & 1) ^ 1u, a.wait_ns)) { ok = false; break; }
         float *pp = sm.part + (tb * kWarps + c) * M * kGroupRows;
+        if (MMA) {
+            const int t = lane & 3, g = lane >> 2;
+            if (t < M)
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+                for (int r = 0; r < 8; ++r) {
+                    pp[t * kGroupRows + 16 * r + g] = yq[r][0];
+                    pp[t * kGroupRows + 16 * r + g + 8] = yq[r][1];
+                }
+        } else {
 #pragma unroll
-            for (int t = 0; t < M; ++t) pp[t * kGroupRows + lane + 32 * r] = yp[r][t];
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int t = 0; t < M; ++t) pp[t * kGroupRows + lane + 32 * r] = yp[r][t];
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.gfull[tb]);
         if (g >= 1 && !reduce_group<M>(a, sm, g - 1, c, lane, rank, G0, yrow)) { ok = false; break; }
@@ -415,13 +573,21 @@ size_t gemv_smem(int M, int S, int ring)
     return static_cast<size_t>(ring) * kRecordBytes + part + red + bars;
 }
 
-const void *gemv_fn(int M)
+const void *gemv_fn(int M, bool mma)
 {
+    if (mma) {
+        switch (M) {
+        case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, true>);
+        case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, true>);
+        case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, true>);
+        default: return reinterpret_cast<const void *>(&gemv_kernel<4, true>);
+        }
+    }
     switch (M) {
-    case 1: return reinterpret_cast<const void *>(&gemv_kernel<1>);
-    case 2: return reinterpret_cast<const void *>(&gemv_kernel<2>);
-    case 3: return reinterpret_cast<const void *>(&gemv_kernel<3>);
-    default: return reinterpret_cast<const void *>(&gemv_kernel<4>);
+    case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, false>);
+    case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, false>);
+    case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, false>);
+    default: return reinterpret_cast<const void *>(&gemv_kernel<4, false>);
     }
 }
 
@@ -442,7 +608,7 @@ int max_active_clusters(int M, int S, size_t smem)
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void *fn = gemv_fn(M);
+    const void *fn = gemv_fn(M, false);
     int n = 0;
     if (set_max_smem(fn, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
@@ -521,9 +687,9 @@ bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
     return true;
 }
 
-cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, cudaStream_t s)
+cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, bool mma, cudaStream_t s)
 {
-    const void *fn = gemv_fn(plan.M);
+    const void *fn = gemv_fn(plan.M, mma);
     cudaError_t e = set_max_smem(fn, plan.smem);
     if (e != cudaSuccess) return e;
     DecodeArgs a = args;

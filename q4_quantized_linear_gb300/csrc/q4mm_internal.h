@@ -114,7 +114,9 @@ struct GemvPlan {
 };
 
 bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan);
-cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, cudaStream_t s);
+// mma: the record-MMA mode (exact fp16 (q - 8) on the warp-level tensor core)
+// instead of fp32 FMAs; the same plan serves both.
+cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, bool mma, cudaStream_t s);
 
 // ------------------------------------------------------------ warp MMA --
 
