@@ -258,9 +258,10 @@ __device__ __forceinline__ void x_load(const float *xrow, int blk, bool live, in
 }
 
 // B fragments of one block from this lane's X values (column g: token g / 2,
-// term g % 2), and the inverse scale of the token this lane's accumulators
-// hold (t).
-__device__ __forceinline__ void x_fragments(const float4 &xa, const float4 &xb, int lane, uint4 &bf, float &su_t)
+// term g % 2), and the inverse of the scale this lane's column took. Lanes
+// 4g .. 4g + 3 (of `lane`, which may be a lane index within a half warp)
+// agree on the scale.
+__device__ __forceinline__ void x_fragments(const float4 &xa, const float4 &xb, int lane, uint4 &bf, float &inv)
 {
     const int g = lane >> 2, t = lane & 3, h = g & 1;
     unsigned mb = max(absmax_bits(xa), absmax_bits(xb));
@@ -278,8 +279,7 @@ __device__ __forceinline__ void x_fragments(const float4 &xa, const float4 &xb, 
     bf.y = split_pair(xb.x * su, xb.z * su, h, fin);   //           16+4t, 18+4t
     bf.z = split_pair(xa.y * su, xa.w * su, h, fin);   // k-step 1: 4t+1, 4t+3
     bf.w = split_pair(xb.y * su, xb.w * su, h, fin);   //           17+4t, 19+4t
-    const float inv = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);
-    su_t = __shfl_sync(0xFFFFFFFFu, inv, 8 * t);       // column 2t: token t's hi term
+    inv = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);
 }
 
 // One record through the tensor core: y[rt][0 / 1] += rows 16 rt + g and
@@ -467,8 +467,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         yrow[t] = t < a.m ? (a.rows ? __ldg(a.rows + t) : t) : 0;
         xr[t] = a.X + static_cast<int64_t>(yrow[t]) * a.ldx;
     }
-    // record-MMA mode: this lane's B column is token (lane / 8)
-    const int col_tok = lane >> 3;
+    // Record-MMA mode: this lane's B column is token (lane / 8). For m <= 2
+    // the live columns are lanes 0-15 only, so X is built in one pass: lanes
+    // 0-15 build block 2p of a pair p and lanes 16-31 block 2p + 1 for the
+    // same columns, handed to lanes 0-15 by shuffles.
+    constexpr bool kOnePass = MMA && M <= 2;
+    const int xb1 = kOnePass ? (lane >> 4) : 0;       // block of the pair this lane builds
+    const int col_tok = kOnePass ? ((lane & 15) >> 3) : (lane >> 3);
     const bool col_live = col_tok < M && col_tok < a.m;
     const float *xcol = a.X + (col_live ? static_cast<int64_t>(a.rows ? __ldg(a.rows + col_tok) : col_tok) * a.ldx : 0);
 
@@ -481,8 +486,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
     float4 xn[2][2];
     if (MMA && ci < ntiles) {
         const int b0 = 2 * (p0 + cj);
-        x_load(xcol, b0, col_live, lane, xn[0][0], xn[0][1]);
-        x_load(xcol, b0 + 1, col_live && b0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
+        if (kOnePass) {
+            x_load(xcol, b0 + xb1, col_live && b0 + xb1 < a.nb, lane, xn[0][0], xn[0][1]);
+        } else {
+            x_load(xcol, b0, col_live, lane, xn[0][0], xn[0][1]);
+            x_load(xcol, b0 + 1, col_live && b0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
+        }
     }
     for (int g = 0; g < ntiles && ok; ++g) {
         const int tb = g & 1;
@@ -502,14 +511,38 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
                 // a missing second block is padding (weights exactly 0) against X = 0
                 uint4 bf[2];
                 float su[2];
-                x_fragments(xn[0][0], xn[0][1], lane, bf[0], su[0]);
-                x_fragments(xn[1][0], xn[1][1], lane, bf[1], su[1]);
+                const int tq = lane & 3;                  // token of this lane's accumulators
+                if (kOnePass) {
+                    uint4 v;
+                    float inv;
+                    x_fragments(xn[0][0], xn[0][1], lane & 15, v, inv);
+                    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+                    uint4 hi;
+                    hi.x = __shfl_down_sync(0xFFFFFFFFu, v.x, 16);
+                    hi.y = __shfl_down_sync(0xFFFFFFFFu, v.y, 16);
+                    hi.z = __shfl_down_sync(0xFFFFFFFFu, v.z, 16);
+                    hi.w = __shfl_down_sync(0xFFFFFFFFu, v.w, 16);
+                    bf[0] = lane < 16 ? v : zero;         // columns 4-7 (tokens 2, 3) are zero
+                    bf[1] = lane < 16 ? hi : zero;
+                    su[0] = __shfl_sync(0xFFFFFFFFu, inv, 8 * tq);        // token tq's hi column
+                    su[1] = __shfl_sync(0xFFFFFFFFu, inv, 16 + 8 * tq);
+                } else {
+                    float inv0, inv1;
+                    x_fragments(xn[0][0], xn[0][1], lane, bf[0], inv0);
+                    x_fragments(xn[1][0], xn[1][1], lane, bf[1], inv1);
+                    su[0] = __shfl_sync(0xFFFFFFFFu, inv0, 8 * tq);
+                    su[1] = __shfl_sync(0xFFFFFFFFu, inv1, 8 * tq);
+                }
                 int ni = ci, nj = cj;
                 step_pos(ni, nj, P);
                 if (ni < ntiles) {
                     const int nb0 = 2 * (p0 + nj);
-                    x_load(xcol, nb0, col_live, lane, xn[0][0], xn[0][1]);
-                    x_load(xcol, nb0 + 1, col_live && nb0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
+                    if (kOnePass) {
+                        x_load(xcol, nb0 + xb1, col_live && nb0 + xb1 < a.nb, lane, xn[0][0], xn[0][1]);
+                    } else {
+                        x_load(xcol, nb0, col_live, lane, xn[0][0], xn[0][1]);
+                        x_load(xcol, nb0 + 1, col_live && nb0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
+                    }
                 }
                 mma_record(rec, bf, su, lane, yq);
             } else {
