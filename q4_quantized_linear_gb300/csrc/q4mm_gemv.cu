@@ -339,12 +339,38 @@ __device__ __forceinline__ void step_pos(int &i, int &j, int P)
     while (j >= P) j -= P, ++i;
 }
 
-// Sum the eight warps' partials of group g for this warp's rows, then meet
-// the cluster's other slices of them and write Y (first CTA) or send them
-// there. Lane l handles row 16 c + (l & 15) and tokens t = l / 16, + 2, ...
+// First CTA of the cluster: add the other slices of group g's rows (landed
+// in its shared memory) to this warp's sums y and write them to Y.
+template <int M>
+__device__ __forceinline__ void write_rows(const DecodeArgs &a, const GSmem &sm, int g, int c, int lane, int G0,
+                                           const int yrow[M], const float y[(M + 1) / 2])
+{
+    const int S = a.S;
+    const int tb = g & 1;
+    const int row = c * kSliceRows + (lane & (kSliceRows - 1));
+    const int t0 = lane >> 4;
+    const int64_t grow = static_cast<int64_t>(G0 + g * a.clusters) * kGroupRows + row;
+    if (grow >= a.n) return;
+#pragma unroll
+    for (int h = 0; h < (M + 1) / 2; ++h) {
+        const int t = t0 + 2 * h;
+        if (t < M && t < a.m) {
+            float v = y[h];
+            for (int r = 1; r < S; ++r) v += sm.red[((tb * (S - 1) + r - 1) * M + t) * kGroupRows + row];
+            a.Y[static_cast<int64_t>(yrow[t]) * a.ldy + grow] = v;
+        }
+    }
+}
+
+// Sum the eight warps' partials of group g for this warp's rows (into y),
+// then meet the cluster's other slices of them and write Y (first CTA) or
+// send them there. Lane l handles row 16 c + (l & 15) and tokens t = l / 16,
+// + 2, ... With `merged` (the group is the CTA's only one) the slices meet
+// through the cluster barrier that ends the kernel instead: no barrier
+// handshake, and the first CTA writes Y after that barrier.
 template <int M>
 __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &sm, int g, int c, int lane, int rank,
-                                             int G0, const int yrow[M])
+                                             int G0, const int yrow[M], bool merged, float y[(M + 1) / 2])
 {
     const int S = a.S;
     const int tb = g & 1;
@@ -352,7 +378,6 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &s
     if (!warp_wait(&sm.gfull[tb], par, a.wait_ns)) return false;
     const int row = c * kSliceRows + (lane & (kSliceRows - 1));
     const int t0 = lane >> 4;
-    float y[(M + 1) / 2];
 #pragma unroll
     for (int h = 0; h < (M + 1) / 2; ++h) {
         const int t = t0 + 2 * h;
@@ -364,7 +389,6 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &s
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.gfree[tb]);
-    const int64_t grow = static_cast<int64_t>(G0 + g * a.clusters) * kGroupRows + row;
     if (rank > 0) {
         // this slice's rows into the first CTA's slot tb, then signal it
         if (g >= 2 && !warp_wait_cluster(&sm.red_free[tb * kWarps + c], par ^ 1u, a.wait_ns)) return false;
@@ -375,21 +399,13 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &s
             const int t = t0 + 2 * h;
             if (t < M) st_cluster_f32(dst + static_cast<uint32_t>(t * kGroupRows * 4), y[h]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_full[tb * kWarps + c]), 0u));
-    } else {
-        if (S > 1 && !warp_wait_cluster(&sm.red_full[tb * kWarps + c], par, a.wait_ns)) return false;
-        if (grow < a.n) {
-#pragma unroll
-            for (int h = 0; h < (M + 1) / 2; ++h) {
-                const int t = t0 + 2 * h;
-                if (t < M && t < a.m) {
-                    float v = y[h];
-                    for (int r = 1; r < S; ++r) v += sm.red[((tb * (S - 1) + r - 1) * M + t) * kGroupRows + row];
-                    a.Y[static_cast<int64_t>(yrow[t]) * a.ldy + grow] = v;
-                }
-            }
+        if (!merged) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&sm.red_full[tb * kWarps + c]), 0u));
         }
+    } else if (!merged) {
+        if (S > 1 && !warp_wait_cluster(&sm.red_full[tb * kWarps + c], par, a.wait_ns)) return false;
+        write_rows<M>(a, sm, g, c, lane, G0, yrow, y);
         if (S > 1) {
             __syncwarp();
             if (lane == 0)
@@ -580,9 +596,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.gfull[tb]);
-        if (g >= 1 && !reduce_group<M>(a, sm, g - 1, c, lane, rank, G0, yrow)) { ok = false; break; }
+        float yg[(M + 1) / 2];
+        if (g >= 1 && !reduce_group<M>(a, sm, g - 1, c, lane, rank, G0, yrow, false, yg)) { ok = false; break; }
     }
-    if (ok && ntiles > 0) ok = reduce_group<M>(a, sm, ntiles - 1, c, lane, rank, G0, yrow);
+    // When every CTA of the grid has a single group, its slices meet through
+    // the closing cluster barrier (measured faster there; with two groups per
+    // CTA, on 14336 x 4096 at m = 3 and 4, slower than the handshake).
+    const bool merged = S > 1 && a.groups <= a.clusters;
+    float ylast[(M + 1) / 2];
+    const bool fin = ok && ntiles > 0;
+    if (fin) ok = reduce_group<M>(a, sm, ntiles - 1, c, lane, rank, G0, yrow, merged, ylast);
     if (!ok) {
         fail(a);
         // A warp that gave up may still have copies landing in its slots
@@ -593,9 +616,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         __syncwarp();
     }
 
-    // every CTA of the cluster stays until the others are done with its
-    // shared memory and barriers
-    if (S > 1) cluster_sync();
+    // Every CTA of the cluster stays until the others are done with its
+    // shared memory and barriers; the barrier also makes the other slices'
+    // rows of the last group, stored before it, visible to the first CTA.
+    if (S > 1) {
+        cluster_sync();
+        if (merged && fin && ok && rank == 0) write_rows<M>(a, sm, ntiles - 1, c, lane, G0, yrow, ylast);
+    }
 }
 
 size_t gemv_smem(int M, int S, int ring)
