@@ -693,13 +693,23 @@ int max_active_clusters(int M, int S, size_t smem)
 
 // Choose the cluster size S (K slices per 128-row group), the number of
 // persistent clusters and the ring depth. Candidates per S: the deepest ring
-// that fits one CTA's shared memory, and the deepest that leaves room for a
-// second CTA on the SM (the next call's, or this call's). The number of
-// clusters is capped by what the device holds at once (a second wave would
-// double the time). Cost, in record times of one SM's share of HBM: the
-// busiest SM's records at the rate its CTAs sustain, plus per-group and
-// per-slice overheads, plus the start-up that cannot overlap the preceding
-// call when no SM has room left for the next call's CTA.
+// that fits one CTA's shared memory and the deepest that leaves room for a
+// second CTA on the SM, neither deeper than the CTA's records need. The
+// number of clusters is capped by what the device holds at once (a second
+// wave would double the time).
+//
+// Costs are in record times of one SM's share of HBM (about 0.1 us on
+// GB300), fitted to graph-replay timings of the record-MMA mode:
+// - Single-group plans (one 128-row group per cluster) come first: their
+//   slices meet through the closing cluster barrier, and on every layer
+//   measured the best plan was one of them. Their cost is the busiest SM's
+//   records (1.5 each with one CTA on the SM, 1.1 each with two), plus the
+//   records a CTA must wait for beyond its ring (three times as dear with a
+//   ring of one record per warp), plus per-slice cluster overheads, plus
+//   the start-up that cannot overlap the preceding call when no SM has room
+//   for the next call's CTA.
+// - Grids with more groups than resident clusters pay the busiest SM's
+//   records at the rate its CTAs sustain and the per-group overheads.
 bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
 {
     if (m < 1 || m > kGemvMaxM || sm_count < 1) return false;
@@ -711,10 +721,15 @@ bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
     GemvPlan best;
     double best_cost = 1e300;
     for (int S = 1; S <= kMaxSlices && S <= np; ++S) {
-        for (int two = 0; two <= 1; ++two) {
+        const int64_t P = ceil_div(np, S);
+        const int need = static_cast<int>(std::min<int64_t>(kMaxRing, std::max<int64_t>(kWarps, ceil_div(P, kWarps) * kWarps)));
+        for (int cand = 0; cand < 4; ++cand) {
+            const int two = cand & 1;
+            const int top = cand < 2 ? need : kMaxRing;    // a ring deeper than the records only helps
+            if (cand >= 2 && top == need) continue;          // a CTA with several groups
             const size_t limit = two ? half : kSmemOptIn;
             int ring = 0;
-            for (int r = kMaxRing; r >= kWarps && ring == 0; r -= kWarps)
+            for (int r = top; r >= kWarps && ring == 0; r -= kWarps)
                 if (gemv_smem(M, S, r) <= limit) ring = r;
             if (ring == 0) continue;
             const size_t smem = gemv_smem(M, S, ring);
@@ -724,13 +739,22 @@ bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
             if (cmax < 1) continue;
             const int64_t clusters = std::min<int64_t>(groups, cmax);
             const int64_t tiles = ceil_div(groups, clusters);
-            const int64_t P = ceil_div(np, S);
             const int64_t ctas = clusters * S;
             const int per_sm = ctas > sm_count ? 2 : 1;
-            const double rate = per_sm == 2 ? 1.0 : (two_fit ? 0.9 : 0.8);
-            const double stream = std::max(static_cast<double>(tiles * P * per_sm) / rate, total / sm_count);
-            const double no_overlap = (!two_fit || per_sm == 2) ? 15.0 : 0.0;
-            const double cost = stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 2.0 : 0.0) + no_overlap;
+            const double no_overlap = (!two_fit || per_sm == 2) ? 10.0 : 0.0;
+            double cost;
+            if (tiles == 1) {
+                const double Pd = static_cast<double>(P);
+                const double work = per_sm == 2 ? 2.0 * Pd * 1.1 : Pd * 1.5;
+                const double starve =
+                    per_sm == 1 && P > ring ? static_cast<double>(P - ring) * (ring <= kWarps ? 3.0 : 1.0) : 0.0;
+                const double slices = S > 1 ? 3.0 + 2.0 * (S - 2) : 0.0;
+                cost = work + starve + slices + no_overlap;
+            } else {
+                const double rate = per_sm == 2 ? 1.0 : (two_fit ? 0.9 : 0.8);
+                const double stream = std::max(static_cast<double>(tiles * P * per_sm) / rate, total / sm_count);
+                cost = 1000.0 + stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 2.0 : 0.0) + 1.5 * no_overlap;
+            }
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.M = M;
