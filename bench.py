@@ -72,11 +72,12 @@ def weight_bytes(n, k):
     return n * (k // 32) * 18
 
 
-def decode_kernel_name(m):
-    """The kernel the library's automatic dispatch runs for m token rows."""
+def decode_kernel_name(m, n=0, sm_count=152):
+    """The kernel the library's automatic dispatch runs for m token rows of
+    an n-row layer."""
     if m > 16:
         return "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)"
-    if m <= 4:
+    if m <= 4 or (m <= 8 and (n + 127) // 128 <= 2 * sm_count):
         return "gemv_kernel<m, true> (q4mm_gemv.cu, whole records per warp on the warp-level MMA)"
     return "mmv_kernel (q4mm_mmv.cu, row-tiled warp-level MMA)"
 
@@ -442,7 +443,7 @@ def native(args):
         },
         "roofline": {
             "bound": "tensor" if tensor else "hbm",
-            "kernel": decode_kernel_name(m),
+            "kernel": decode_kernel_name(m, n, torch.cuda.get_device_properties(local).multi_processor_count),
             "achieved": achieved,
             "peak": peak,
             "unit": unit,

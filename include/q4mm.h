@@ -220,8 +220,10 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
  * runs is a performance choice. The pages bound decode by the weight read
  * (golem, "Qwen3.8 drafts its own next token"), so the kernels differ in how
  * few instructions they spend per weight byte:
- *   Q4_DECODE_AUTO       the library's choice for each m (default): record
- *                        MMA for m <= 4, warp-MMA above;
+ *   Q4_DECODE_AUTO       the library's choice for each call (default):
+ *                        record MMA for m <= 4, and for m <= 8 on layers of
+ *                        at most two 128-row groups per SM; warp-MMA
+ *                        otherwise;
  *   Q4_DECODE_WARP_MMA   CUDA cores dequantise to exact fp16 (q - 8), the
  *                        warp-level MMA (mma.sync) multiplies by X split into
  *                        fp16 hi + lo, d is applied in fp32 per block;
@@ -231,7 +233,7 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
  *                        split into fp16 hi + lo, tcgen05.mma;
  *   Q4_DECODE_RECORD_MMA each warp takes whole records: exact fp16 (q - 8)
  *                        times X split per block into fp16 hi + lo on the
- *                        warp-level MMA, d applied in fp32 per block (m <= 4;
+ *                        warp-level MMA, d applied in fp32 per block (m <= 8;
  *                        wider calls take Q4_DECODE_WARP_MMA).
  * The setting is kept per process and applies to launches made after the
  * call. Other values are refused with Q4_ERR_INVALID_ARG. */

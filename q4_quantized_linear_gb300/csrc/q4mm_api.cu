@@ -178,11 +178,17 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         a.groups = static_cast<int>(ceil_div(n, kGroupRows));
         a.prefetch_w = g_prefetch_w.load();
         int kind = g_decode_kernel.load();
-        // measured on GB300 (graph replays, weights cycled beyond L2): whole
+        // Measured on GB300 (graph replays, weights cycled beyond L2): whole
         // records per warp on the warp-level MMA are fastest for m <= 4 on
-        // every layer measured, the row-tiled warp-MMA kernel above
-        if (kind == Q4_DECODE_AUTO) kind = m <= kGemvMaxM ? Q4_DECODE_RECORD_MMA : Q4_DECODE_WARP_MMA;
-        if ((kind == Q4_DECODE_CUDA_CORE || kind == Q4_DECODE_RECORD_MMA) && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;
+        // every layer measured, and for m = 5..8 on layers of up to two
+        // 128-row groups per SM (on the 151936-row logit layer the row-tiled
+        // warp-MMA kernel is faster there); the warp-MMA kernel above m = 8.
+        if (kind == Q4_DECODE_AUTO) {
+            const bool whole = m <= kGemvMaxM || (m <= kRecordMmaMaxM && a.groups <= 2 * dev.sm_count);
+            kind = whole ? Q4_DECODE_RECORD_MMA : Q4_DECODE_WARP_MMA;
+        }
+        if (kind == Q4_DECODE_CUDA_CORE && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;
+        if (kind == Q4_DECODE_RECORD_MMA && m > kRecordMmaMaxM) kind = Q4_DECODE_WARP_MMA;
         if (kind == Q4_DECODE_WARP_MMA) {
             MmvPlan mp;
             if (!plan_mmv(m, k, n, dev.sm_count, &mp)) return Q4_ERR_INVALID_ARG;

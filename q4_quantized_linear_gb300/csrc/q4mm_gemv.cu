@@ -282,10 +282,12 @@ __device__ __forceinline__ void x_fragments(const float4 &xa, const float4 &xb, 
     inv = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);
 }
 
-// One record through the tensor core: y[rt][0 / 1] += rows 16 rt + g and
-// 16 rt + g + 8, token t (lane 4g + t).
-__device__ __forceinline__ void mma_record(const uint8_t *rec, const uint4 bf[2], const float su[2], int lane,
-                                           float y[8][2])
+// One record through the tensor core: y[nt][rt][0 / 1] += rows 16 rt + g
+// and 16 rt + g + 8, token 4 nt + t (lane 4g + t). The weights of a row tile
+// are turned into fp16 once for all NT column tiles.
+template <int NT>
+__device__ __forceinline__ void mma_record(const uint8_t *rec, const uint4 bf[NT][2], const float su[NT][2],
+                                           int lane, float y[NT][8][2])
 {
     const int g = lane >> 2, t = lane & 3;
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -310,13 +312,15 @@ __device__ __forceinline__ void mma_record(const uint8_t *rec, const uint4 bf[2]
         const float2 d0 = __half22float2(*reinterpret_cast<const __half2 *>(&sc0));   // row g: block 0, 1
         const float2 d1 = __half22float2(*reinterpret_cast<const __half2 *>(&sc1));   // row g + 8
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            float D[4];
-            mma_f16(D, A[b][0], bf[b].x, bf[b].y, zero4);
-            mma_f16(D, A[b][1], bf[b].z, bf[b].w, D);
-            y[rt][0] = fmaf((b ? d0.y : d0.x) * su[b], D[0] + D[1], y[rt][0]);
-            y[rt][1] = fmaf((b ? d1.y : d1.x) * su[b], D[2] + D[3], y[rt][1]);
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float D[4];
+                mma_f16(D, A[b][0], bf[nt][b].x, bf[nt][b].y, zero4);
+                mma_f16(D, A[b][1], bf[nt][b].z, bf[nt][b].w, D);
+                y[nt][rt][0] = fmaf((b ? d0.y : d0.x) * su[nt][b], D[0] + D[1], y[nt][rt][0]);
+                y[nt][rt][1] = fmaf((b ? d1.y : d1.x) * su[nt][b], D[2] + D[3], y[nt][rt][1]);
+            }
     }
 }
 
@@ -483,15 +487,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         yrow[t] = t < a.m ? (a.rows ? __ldg(a.rows + t) : t) : 0;
         xr[t] = a.X + static_cast<int64_t>(yrow[t]) * a.ldx;
     }
-    // Record-MMA mode: this lane's B column is token (lane / 8). For m <= 2
-    // the live columns are lanes 0-15 only, so X is built in one pass: lanes
-    // 0-15 build block 2p of a pair p and lanes 16-31 block 2p + 1 for the
-    // same columns, handed to lanes 0-15 by shuffles.
+    // Record-MMA mode: in column tile nt, this lane's B column is token
+    // 4 nt + lane / 8. For m <= 2 the live columns are lanes 0-15 only, so X
+    // is built in one pass: lanes 0-15 build block 2p of a pair p and lanes
+    // 16-31 block 2p + 1 for the same columns, handed to lanes 0-15 by
+    // shuffles. With one column tile a warp's X values are loaded one record
+    // ahead; with two (m = 5..8) they are loaded where they are used (L1).
+    constexpr int NT = MMA ? (M + 3) / 4 : 1;
     constexpr bool kOnePass = MMA && M <= 2;
     const int xb1 = kOnePass ? (lane >> 4) : 0;       // block of the pair this lane builds
     const int col_tok = kOnePass ? ((lane & 15) >> 3) : (lane >> 3);
     const bool col_live = col_tok < M && col_tok < a.m;
     const float *xcol = a.X + (col_live ? static_cast<int64_t>(a.rows ? __ldg(a.rows + col_tok) : col_tok) * a.ldx : 0);
+    const int col_tok2 = 4 + (lane >> 3);               // second column tile (NT = 2)
+    const bool col_live2 = NT > 1 && col_tok2 < M && col_tok2 < a.m;
+    const float *xcol2 =
+        a.X + (col_live2 ? static_cast<int64_t>(a.rows ? __ldg(a.rows + col_tok2) : col_tok2) * a.ldx : 0);
 
     bool ok = true;
     int s = c;
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
     // record-MMA mode: X values of the warp's next record, loaded one record
     // ahead so that their latency hides behind the current record's work
     float4 xn[2][2];
-    if (MMA && ci < ntiles) {
+    if (MMA && NT == 1 && ci < ntiles) {
         const int b0 = 2 * (p0 + cj);
         if (kOnePass) {
             x_load(xcol, b0 + xb1, col_live && b0 + xb1 < a.nb, lane, xn[0][0], xn[0][1]);
@@ -516,19 +527,33 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int t = 0; t < M; ++t) yp[r][t] = 0.0f;
-        float yq[8][2];
+        float yq[NT][8][2];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) yq[r][0] = yq[r][1] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) yq[nt][r][0] = yq[nt][r][1] = 0.0f;
         for (; ci == g; step_pos(ci, cj, P)) {
             if (!warp_wait(&sm.full_w[s], ph, a.wait_ns)) { ok = false; break; }
             const uint8_t *rec = sm.w + static_cast<size_t>(s) * kRecordBytes;
             const int b0 = 2 * (p0 + cj);
             if (MMA) {
                 // a missing second block is padding (weights exactly 0) against X = 0
-                uint4 bf[2];
-                float su[2];
-                const int tq = lane & 3;                  // token of this lane's accumulators
-                if (kOnePass) {
+                uint4 bf[NT][2];
+                float su[NT][2];
+                const int tq = lane & 3;                  // token of this lane's accumulators, per tile
+                if (NT > 1) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            float4 xa, xb;
+                            x_load(nt ? xcol2 : xcol, b0 + b, (nt ? col_live2 : col_live) && b0 + b < a.nb, lane, xa,
+                                   xb);
+                            float inv;
+                            x_fragments(xa, xb, lane, bf[nt][b], inv);
+                            su[nt][b] = __shfl_sync(0xFFFFFFFFu, inv, 8 * tq);
+                        }
+                } else if (kOnePass) {
                     uint4 v;
                     float inv;
                     x_fragments(xn[0][0], xn[0][1], lane & 15, v, inv);
@@ -538,20 +563,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
                     hi.y = __shfl_down_sync(0xFFFFFFFFu, v.y, 16);
                     hi.z = __shfl_down_sync(0xFFFFFFFFu, v.z, 16);
                     hi.w = __shfl_down_sync(0xFFFFFFFFu, v.w, 16);
-                    bf[0] = lane < 16 ? v : zero;         // columns 4-7 (tokens 2, 3) are zero
-                    bf[1] = lane < 16 ? hi : zero;
-                    su[0] = __shfl_sync(0xFFFFFFFFu, inv, 8 * tq);        // token tq's hi column
-                    su[1] = __shfl_sync(0xFFFFFFFFu, inv, 16 + 8 * tq);
+                    bf[0][0] = lane < 16 ? v : zero;      // columns 4-7 (tokens 2, 3) are zero
+                    bf[0][1] = lane < 16 ? hi : zero;
+                    su[0][0] = __shfl_sync(0xFFFFFFFFu, inv, 8 * tq);     // token tq's hi column
+                    su[0][1] = __shfl_sync(0xFFFFFFFFu, inv, 16 + 8 * tq);
                 } else {
                     float inv0, inv1;
-                    x_fragments(xn[0][0], xn[0][1], lane, bf[0], inv0);
-                    x_fragments(xn[1][0], xn[1][1], lane, bf[1], inv1);
-                    su[0] = __shfl_sync(0xFFFFFFFFu, inv0, 8 * tq);
-                    su[1] = __shfl_sync(0xFFFFFFFFu, inv1, 8 * tq);
+                    x_fragments(xn[0][0], xn[0][1], lane, bf[0][0], inv0);
+                    x_fragments(xn[1][0], xn[1][1], lane, bf[0][1], inv1);
+                    su[0][0] = __shfl_sync(0xFFFFFFFFu, inv0, 8 * tq);
+                    su[0][1] = __shfl_sync(0xFFFFFFFFu, inv1, 8 * tq);
                 }
                 int ni = ci, nj = cj;
                 step_pos(ni, nj, P);
-                if (ni < ntiles) {
+                if (NT == 1 && ni < ntiles) {
                     const int nb0 = 2 * (p0 + nj);
                     if (kOnePass) {
                         x_load(xcol, nb0 + xb1, col_live && nb0 + xb1 < a.nb, lane, xn[0][0], xn[0][1]);
@@ -560,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
                         x_load(xcol, nb0 + 1, col_live && nb0 + 1 < a.nb, lane, xn[1][0], xn[1][1]);
                     }
                 }
-                mma_record(rec, bf, su, lane, yq);
+                mma_record<NT>(rec, bf, su, lane, yq);
             } else {
                 uint32_t sc[4];
 #pragma unroll
@@ -581,13 +606,17 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
         if (g >= 2 && !warp_wait(&sm.gfree[tb], ((g >> 1) & 1) ^ 1u, a.wait_ns)) { ok = false; break; }
         float *pp = sm.part + (tb * kWarps + c) * M * kGroupRows;
         if (MMA) {
-            const int t = lane & 3, g = lane >> 2;
-            if (t < M)
+            const int g = lane >> 2;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    pp[t * kGroupRows + 16 * r + g] = yq[r][0];
-                    pp[t * kGroupRows + 16 * r + g + 8] = yq[r][1];
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                const int t = 4 * nt + (lane & 3);
+                if (t < M)
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        pp[t * kGroupRows + 16 * r + g] = yq[nt][r][0];
+                        pp[t * kGroupRows + 16 * r + g + 8] = yq[nt][r][1];
+                    }
+            }
         } else {
 #pragma unroll
             for (int r = 0; r < 4; ++r)
@@ -640,7 +669,11 @@ const void *gemv_fn(int M, bool mma)
         case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, true>);
         case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, true>);
         case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, true>);
-        default: return reinterpret_cast<const void *>(&gemv_kernel<4, true>);
+        case 4: return reinterpret_cast<const void *>(&gemv_kernel<4, true>);
+        case 5: return reinterpret_cast<const void *>(&gemv_kernel<5, true>);
+        case 6: return reinterpret_cast<const void *>(&gemv_kernel<6, true>);
+        case 7: return reinterpret_cast<const void *>(&gemv_kernel<7, true>);
+        default: return reinterpret_cast<const void *>(&gemv_kernel<8, true>);
         }
     }
     switch (M) {
@@ -668,7 +701,7 @@ int max_active_clusters(int M, int S, size_t smem)
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void *fn = gemv_fn(M, false);
+    const void *fn = gemv_fn(M, M > kGemvMaxM);        // the CUDA-core mode is built for m <= 4 only
     int n = 0;
     if (set_max_smem(fn, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
@@ -712,7 +745,7 @@ int max_active_clusters(int M, int S, size_t smem)
 //   records at the rate its CTAs sustain and the per-group overheads.
 bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
 {
-    if (m < 1 || m > kGemvMaxM || sm_count < 1) return false;
+    if (m < 1 || m > kRecordMmaMaxM || sm_count < 1) return false;
     const int M = static_cast<int>(m);
     const int64_t groups = ceil_div(n, kGroupRows);
     const int64_t np = ceil_div(k, kPairK);
