@@ -495,7 +495,13 @@ bool plan_mmv(int64_t m, int64_t k, int64_t n, int sm_count, MmvPlan *plan)
             const double recs = static_cast<double>(tiles * P);   // records per CTA
             const double stream = std::max(recs * per_sm / rate, total / sm_count);
             const double no_overlap = (!two_fit || per_sm == 2) ? 15.0 : 0.0;
-            const double cost = stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 12.0 : 0.0) + no_overlap;
+            // a CTA with several groups reduces each through the cluster
+            // handshake at the end of the next one: measured about 3 us more
+            // than a grid of single-group CTAs (9728 x 2560 at m = 16: 23.8 us
+            // with two groups per CTA, 15.9 us with one)
+            const double groups_cost = tiles > 1 ? 30.0 : 0.0;
+            const double cost =
+                stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 12.0 : 0.0) + no_overlap + groups_cost;
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.NT = NT;
