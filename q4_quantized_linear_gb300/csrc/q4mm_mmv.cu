@@ -495,13 +495,20 @@ bool plan_mmv(int64_t m, int64_t k, int64_t n, int sm_count, MmvPlan *plan)
             const double recs = static_cast<double>(tiles * P);   // records per CTA
             const double stream = std::max(recs * per_sm / rate, total / sm_count);
             const double no_overlap = (!two_fit || per_sm == 2) ? 15.0 : 0.0;
-            // a CTA with several groups reduces each through the cluster
-            // handshake at the end of the next one: measured about 3 us more
+            // A CTA with several groups reduces each through the cluster
+            // handshake at the end of the next one. Measured: about 3 us more
             // than a grid of single-group CTAs (9728 x 2560 at m = 16: 23.8 us
-            // with two groups per CTA, 15.9 us with one)
-            const double groups_cost = tiles > 1 ? 30.0 : 0.0;
-            const double cost =
-                stream + 0.5 * static_cast<double>(tiles) + (S > 1 ? 12.0 : 0.0) + no_overlap + groups_cost;
+            // with two groups per CTA, 15.9 us with one), and per group about
+            // 5 + 6 S record times (151936 x 2560 at m = 16: 132 us at S = 1,
+            // 297 us at S = 8 with 33 groups per CTA).
+            const double groups_cost =
+                tiles > 1 ? 30.0 + static_cast<double>(tiles) * (5.0 + 6.0 * S) : 0.5;
+            // a ring of 4 records does not cover the weight stream's latency
+            // (14336 x 4096 at m = 9: one group per CTA with a ring of 4,
+            // 32.5 us; two groups with a ring of 12, 27.7 us); a ring of 6
+            // measured fine (9728 x 2560 at m = 9: 13.2 us)
+            const double starve = ring <= 4 ? recs * (8 - ring) * 0.4 / per_sm : 0.0;
+            const double cost = stream + (S > 1 ? 12.0 : 0.0) + no_overlap + groups_cost + starve;
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.NT = NT;
