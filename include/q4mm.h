@@ -233,8 +233,7 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
  *                        split into fp16 hi + lo, tcgen05.mma;
  *   Q4_DECODE_RECORD_MMA each warp takes whole records: exact fp16 (q - 8)
  *                        times X split per block into fp16 hi + lo on the
- *                        warp-level MMA, d applied in fp32 per block (m <= 8;
- *                        wider calls take Q4_DECODE_WARP_MMA).
+ *                        warp-level MMA, d applied in fp32 per block (m <= 16).
  * The setting is kept per process and applies to launches made after the
  * call. Other values are refused with Q4_ERR_INVALID_ARG. */
 #define Q4_DECODE_AUTO 0

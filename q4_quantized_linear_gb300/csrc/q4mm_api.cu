@@ -182,9 +182,11 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         // records per warp on the warp-level MMA are fastest for m <= 4 on
         // every layer measured, and for m = 5..8 on layers of up to two
         // 128-row groups per SM (on the 151936-row logit layer the row-tiled
-        // warp-MMA kernel is faster there); the warp-MMA kernel above m = 8.
+        // warp-MMA kernel is faster there); the warp-MMA kernel above m = 8
+        // (the record-MMA mode, built up to m = 16, was slower at m = 16 on
+        // 14336 x 4096, 2560 x 9728 and 151936 x 2560).
         if (kind == Q4_DECODE_AUTO) {
-            const bool whole = m <= kGemvMaxM || (m <= kRecordMmaMaxM && a.groups <= 2 * dev.sm_count);
+            const bool whole = m <= kGemvMaxM || (m <= 8 && a.groups <= 2 * dev.sm_count);
             kind = whole ? Q4_DECODE_RECORD_MMA : Q4_DECODE_WARP_MMA;
         }
         if (kind == Q4_DECODE_CUDA_CORE && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;

@@ -421,7 +421,7 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &s
 }
 
 template <int M, bool MMA>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, c = tid >> 5, lane = tid & 31;
@@ -492,17 +492,23 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
     // is built in one pass: lanes 0-15 build block 2p of a pair p and lanes
     // 16-31 block 2p + 1 for the same columns, handed to lanes 0-15 by
     // shuffles. With one column tile a warp's X values are loaded one record
-    // ahead; with two (m = 5..8) they are loaded where they are used (L1).
+    // ahead; with more (m = 5..16) they are loaded where they are used (L1).
     constexpr int NT = MMA ? (M + 3) / 4 : 1;
     constexpr bool kOnePass = MMA && M <= 2;
     const int xb1 = kOnePass ? (lane >> 4) : 0;       // block of the pair this lane builds
     const int col_tok = kOnePass ? ((lane & 15) >> 3) : (lane >> 3);
     const bool col_live = col_tok < M && col_tok < a.m;
     const float *xcol = a.X + (col_live ? static_cast<int64_t>(a.rows ? __ldg(a.rows + col_tok) : col_tok) * a.ldx : 0);
-    const int col_tok2 = 4 + (lane >> 3);               // second column tile (NT = 2)
-    const bool col_live2 = NT > 1 && col_tok2 < M && col_tok2 < a.m;
-    const float *xcol2 =
-        a.X + (col_live2 ? static_cast<int64_t>(a.rows ? __ldg(a.rows + col_tok2) : col_tok2) * a.ldx : 0);
+    // further column tiles (NT > 1): token 4 nt + lane / 8
+    const float *xcolt[NT];
+    bool livet[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int tok = 4 * nt + (lane >> 3);
+        livet[nt] = nt > 0 ? (tok < M && tok < a.m) : col_live;
+        xcolt[nt] = nt > 0 ? a.X + (livet[nt] ? static_cast<int64_t>(a.rows ? __ldg(a.rows + tok) : tok) * a.ldx : 0)
+                           : xcol;
+    }
 
     bool ok = true;
     int s = c;
@@ -547,8 +553,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const DecodeArgs a)
 #pragma unroll
                         for (int b = 0; b < 2; ++b) {
                             float4 xa, xb;
-                            x_load(nt ? xcol2 : xcol, b0 + b, (nt ? col_live2 : col_live) && b0 + b < a.nb, lane, xa,
-                                   xb);
+                            x_load(xcolt[nt], b0 + b, livet[nt] && b0 + b < a.nb, lane, xa, xb);
                             float inv;
                             x_fragments(xa, xb, lane, bf[nt][b], inv);
                             su[nt][b] = __shfl_sync(0xFFFFFFFFu, inv, 8 * tq);
@@ -673,7 +678,15 @@ const void *gemv_fn(int M, bool mma)
         case 5: return reinterpret_cast<const void *>(&gemv_kernel<5, true>);
         case 6: return reinterpret_cast<const void *>(&gemv_kernel<6, true>);
         case 7: return reinterpret_cast<const void *>(&gemv_kernel<7, true>);
-        default: return reinterpret_cast<const void *>(&gemv_kernel<8, true>);
+        case 8: return reinterpret_cast<const void *>(&gemv_kernel<8, true>);
+        case 9: return reinterpret_cast<const void *>(&gemv_kernel<9, true>);
+        case 10: return reinterpret_cast<const void *>(&gemv_kernel<10, true>);
+        case 11: return reinterpret_cast<const void *>(&gemv_kernel<11, true>);
+        case 12: return reinterpret_cast<const void *>(&gemv_kernel<12, true>);
+        case 13: return reinterpret_cast<const void *>(&gemv_kernel<13, true>);
+        case 14: return reinterpret_cast<const void *>(&gemv_kernel<14, true>);
+        case 15: return reinterpret_cast<const void *>(&gemv_kernel<15, true>);
+        default: return reinterpret_cast<const void *>(&gemv_kernel<16, true>);
         }
     }
     switch (M) {

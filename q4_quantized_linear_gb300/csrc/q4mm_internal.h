@@ -104,7 +104,7 @@ cudaError_t launch_decode(const DecodePlan &plan, const DecodeArgs &args, cudaSt
 // Widest call the CUDA-core GEMV kernel is built for.
 constexpr int kGemvMaxM = 4;
 // Widest call the record-MMA mode of the same kernel is built for.
-constexpr int kRecordMmaMaxM = 8;
+constexpr int kRecordMmaMaxM = 16;
 
 struct GemvPlan {
     int M = 1;             // token rows (the kernel instance)

@@ -63,8 +63,7 @@ def once_for_prefill(decode_kernel, m):
         pytest.skip("prefill case: decode kernel irrelevant")
     if decode_kernel == "cuda_core" and m > 4:
         pytest.skip("this kernel serves m <= 4")
-    if decode_kernel == "record_mma" and m > 8:
-        pytest.skip("this kernel serves m <= 8")
+
 
 
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 8, 9, 13, 16])
@@ -85,6 +84,7 @@ def test_decode_parity(q4lib, oracle_mod, decode_kernel, m, n, k):
     ("warp_mma", 1, 9728, 2560, 1e-4), ("warp_mma", 4, 2560, 9728, 1e-4),
     ("record_mma", 1, 9728, 2560, 1e-4), ("record_mma", 3, 14336, 4096, 1e-4),
     ("record_mma", 6, 2560, 9728, 1e-4), ("record_mma", 8, 14336, 4096, 1e-4),
+    ("record_mma", 13, 9728, 2560, 1e-4), ("record_mma", 16, 1000, 2080, 1e-4),
     ("warp_mma", 9, 14336, 4096, 1e-4), ("warp_mma", 16, 1000, 2080, 1e-4)])
 def test_decode_kernel_accuracy_margin(q4lib, oracle_mod, kind, m, n, k, rtol):
     """The CUDA-core kernel forms (q - 8) exactly and multiplies fp32 X
