@@ -94,13 +94,27 @@ def load_peaks():
         return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def kernel_source_hash():
+_COMMENT = re.compile(r"/\*.*?\*/|//[^\n]*", re.S)
+
+
+def source_code_hash(texts):
+    """Hash of (file name, code) pairs with comments and blank space removed,
+    so that a profile taken on the same code stays valid across comment
+    edits."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "q4_quantized_linear_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+    for name, text in sorted(texts):
+        code = " ".join(_COMMENT.sub(" ", text).split())
+        h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "q4_quantized_linear_gb300", "csrc")
+    texts = []
+    for name in os.listdir(csrc):
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            texts.append((name, f.read()))
+    return source_code_hash(texts)
 
 
 def profiled_traffic(kind):

@@ -1,13 +1,15 @@
-// q4mm_gemv.cu -- the CUDA-core kernel for the narrowest decode calls, m = 1
-// to 4 token rows: the decode step (m = 1) and small continuous batches
-// (golem, "Several conversations, one pass"; golem-server, "Several
-// conversations, in one pass"). The pages bound this case by the weight read
-// (golem: two columns cost what one did; goinfer ch. 10, "What the kernels
-// are": the quantised mat-vec is the decode workhorse), so the design goal is
-// to consume a packed record at the rate one SM's share of HBM delivers it
-// with as few instructions as possible.
+// q4mm_gemv.cu -- the decode kernel in which each warp takes whole packed
+// records, for the decode step (m = 1) and small continuous batches (golem,
+// "Several conversations, one pass"; golem-server, "Several conversations, in
+// one pass"). The pages bound this case by the weight read (golem: two
+// columns cost what one did; goinfer ch. 10, "What the kernels are": the
+// quantised mat-vec is the decode workhorse), so the design goal is to
+// consume a packed record at the rate one SM's share of HBM delivers it with
+// as few instructions as possible. Two modes share the warps, ring and
+// reductions: fp32 FMAs on the CUDA cores (m <= 4, below) and the record-MMA
+// mode on the warp-level tensor core (m <= 16, further down).
 //
-// Arithmetic. A weight is (q - 8) * d. One lop3 per weight ORs the nibble,
+// CUDA-core arithmetic. A weight is (q - 8) * d. One lop3 per weight ORs the nibble,
 // left where it lies in its 32-bit word (bit offset s <= 16), into the fp32
 // pattern of 2^23, giving exactly 2^23 + q * 2^s. One fp32 FMA per weight,
 // v * 2^-s - (2^(23-s) + 8), gives (q - 8) exactly. A second FMA per weight
@@ -24,18 +26,20 @@
 // (DSMEM), summed in slice order, so results are bitwise reproducible and no
 // global scratch is used.
 //
-// Warp roles: eight warps per CTA, all alike (two CTAs fit on an SM).
-// Warp c owns the records u = c (mod 8) of the CTA's sequence (its groups x
-// its pairs, in that order) and the ring slots they pass through, R / 8 of
-// them: lane 0 refills a slot with a 1-D bulk copy of the record R places
-// ahead as soon as the warp has read it, so every barrier has one waiter and
-// no copy is in flight when the CTA exits. Lane l owns rows l, l + 32, l + 64
-// and l + 96 of a record: every shared-memory load is 512 contiguous bytes
-// per warp (conflict-free) and every X value a thread loads (a broadcast,
-// L1-resident) serves four rows. At the end of a group each warp leaves its
-// partial rows in shared memory; one group later (so that no warp waits for
-// the slowest), warp c sums the eight partials of rows 16c .. 16c + 15 in
-// order, and then the cluster's slices of those rows, and writes Y. Every
+// Warp roles: eight warps per CTA, all alike (two CTAs fit on an SM up to
+// m = 8). Warp c owns the records u = c (mod 8) of the CTA's sequence (its
+// groups x its pairs, in that order) and the ring slots they pass through,
+// R / 8 of them: lane 0 refills a slot with a 1-D bulk copy of the record R
+// places ahead as soon as the warp has read it, so every barrier has one
+// waiter and no copy is in flight when the CTA exits. In the CUDA-core mode
+// lane l owns rows l, l + 32, l + 64 and l + 96 of a record: every
+// shared-memory load is 512 contiguous bytes per warp (conflict-free) and
+// every X value a thread loads (a broadcast, L1-resident) serves four rows.
+// At the end of a group each warp leaves its partial rows in shared memory;
+// one group later (so that no warp waits for the slowest), warp c sums the
+// eight partials of rows 16c .. 16c + 15 in order, and then the cluster's
+// slices of those rows, and writes Y. When every CTA has a single group, the
+// slices meet through the kernel's closing cluster barrier instead. Every
 // wait is bounded and warp-uniform.
 #include <algorithm>
 #include <cuda_runtime.h>
@@ -204,10 +208,11 @@ __device__ __forceinline__ void gemv_block(const uint8_t *qs, uint32_t dsh, cons
 }
 
 // ------------------------------------------------------------------------
-// Record-MMA mode (m <= 4): the same warps, ring and reductions, but a warp
+// Record-MMA mode (m <= 16): the same warps, ring and reductions, but a warp
 // turns its record's nibbles into exact fp16 (q - 8) (lop3 magic and one fp16
 // FMA per two weights) and multiplies them by X on the tensor core with
-// mma.sync m16n8k16, 16 rows at a time. The MMA's K index is a permutation of
+// mma.sync m16n8k16, 16 rows at a time, in (m + 3) / 4 column tiles of four
+// tokens. The MMA's K index is a permutation of
 // a block's elements chosen so that thread (g, t) of the warp (lane 4g + t)
 // takes its A registers straight from word t of its rows' 16 nibble bytes;
 // X's B fragments use the same permutation. Column g of the 8 is token g / 2,
