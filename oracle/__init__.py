@@ -13,6 +13,11 @@ Functions and the passages they follow:
       Also returns B = sum |x_i w_i|, the magnitude the tolerances scale by.
   fp16_to_double -- IEEE 754 binary16 decode of the block scale.
   dequant_matrix -- the dense fp64 weight matrix (tiny shapes).
+  matmul_w4a8 / quantize_x_w4a8 -- the activation-quantised variant: X
+      coded per 32-element block to int8 (round-half-even of x * 127 / amax,
+      scale amax / 127), integer dot products, fp64 outer sums (goinfer ch.
+      10 "Which kernel runs is a runtime decision"; rembed "Architecture",
+      "int8 quantization"; the coding rule is this oracle's reading).
   pack_reference -- byte-exact reference of the CUDA library's packed layout
       (goinfer ch. 10 "Making Go fast enough": weights repacked for the
       kernel's access order), written from the layout's specification.
@@ -74,6 +79,10 @@ def _load():
         lib.q4o_pack_reference.argtypes = [P, I64, I64, P]
         lib.q4o_pack_reference.restype = ctypes.c_int
         lib.q4o_num_threads.restype = ctypes.c_int
+        lib.q4o_quantize_x_w4a8.argtypes = [P, I64, I64, P, P, P]
+        lib.q4o_quantize_x_w4a8.restype = ctypes.c_int
+        lib.q4o_matmul_w4a8.argtypes = [P, P, I64, I64, I64, P, P, ctypes.c_int]
+        lib.q4o_matmul_w4a8.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -157,3 +166,29 @@ def pack_reference(blocks: np.ndarray, n: int, k: int) -> np.ndarray:
     if _load().q4o_pack_reference(_ptr(blocks), n, k, _ptr(out)) != 0:
         raise RuntimeError("q4o_pack_reference failed")
     return out
+
+
+def quantize_x_w4a8(X: np.ndarray, k: int):
+    """int8 codes [m x k], fp32 scales [m x k/32] and per-row non-finite flags."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    m = X.shape[0]
+    codes = np.zeros((m, k), dtype=np.int8)
+    scales = np.zeros((m, k // 32), dtype=np.float32)
+    bad = np.zeros(m, dtype=np.int32)
+    rc = _load().q4o_quantize_x_w4a8(_ptr(X), m, k, _ptr(codes), _ptr(scales), _ptr(bad))
+    if rc != 0:
+        raise ValueError("bad sizes")
+    return codes, scales, bad.astype(bool)
+
+
+def matmul_w4a8(blocks: np.ndarray, X: np.ndarray, n: int, k: int, nthreads: int = 0):
+    """(Y, B8): the W4A8 product and the per-element magnitude sum of its block terms."""
+    blocks = _check_blocks(blocks, n, k)
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    m = X.shape[0]
+    Y = np.zeros((m, n), dtype=np.float64)
+    B = np.zeros((m, n), dtype=np.float64)
+    rc = _load().q4o_matmul_w4a8(_ptr(blocks), _ptr(X), m, k, n, _ptr(Y), _ptr(B), nthreads)
+    if rc != 0:
+        raise ValueError("bad sizes")
+    return Y, B

@@ -54,6 +54,11 @@ enum {
     MUT_SIGNED_BOUND = 8,        /* B summed without the absolute value */
     MUT_NEGATED = 9,             /* w = (8 - q) * d */
     MUT_X_TRANSPOSED = 10,       /* X read as [k x m] */
+    MUT_A8_ROUND_AWAY = 11,      /* W4A8 codes rounded half away from zero */
+    MUT_A8_SCALE_128 = 12,       /* W4A8 codes and scale on 128 instead of 127 */
+    MUT_A8_ROW_SCALE = 13,       /* W4A8 amax over the whole row, not the block */
+    MUT_A8_TRUNCATE = 14,        /* W4A8 codes truncated toward zero */
+    MUT_A8_NO_OFFSET = 15,       /* W4A8 integer dot without the -8 */
     MUT_COUNT
 };
 
@@ -294,4 +299,110 @@ int q4o_num_threads(void)
 #else
     return 1;
 #endif
+}
+
+/*
+ * W4A8: the activation-quantised variant, in which the inner products run on
+ * integers. goinfer ch. 10 ("Which kernel runs is a runtime decision") names
+ * the canonical quantized dot product that integer-dot hardware runs, and the
+ * rembed "Architecture" page ("int8 quantization") quantises activations so
+ * that the dot product is an integer one, checked bit-exactly against an
+ * integer reference. Neither page prints the rule for the activation codes;
+ * the reading taken here is the plainest symmetric one, per 32-element block
+ * of an X row (the Q4_0 block of the weights it meets):
+ *
+ *   amax     = max_i |x_i|                       (fp32, exact)
+ *   s        = amax / 127                        (fp32, one IEEE division)
+ *   c_i      = round-half-even(x_i * (127 / amax)) (fp32 product and quotient)
+ *
+ * so |c_i| <= 127; a block with amax = 0 has every c_i = 0 and s = 0. A row
+ * of X holding a NaN or an infinity gives NaN in every output of that row.
+ * Then, with q the weight nibbles and d the weight block scales,
+ *
+ *   Y[t][j]  = sum_b d(j,b) * s(t,b) * sum_i (q(j,b,i) - 8) * c(t,b,i)
+ *   B8[t][j] = sum_b |d(j,b) * s(t,b) * sum_i (q(j,b,i) - 8) * c(t,b,i)|
+ *
+ * the inner sums exact in integers, the outer ones in fp64 in block order.
+ */
+
+/* Codes and scales of X: codes [m x k], scales [m x k/32], bad [m]. */
+int q4o_quantize_x_w4a8(const float *X, int64_t m, int64_t k, int8_t *codes, float *scales, int *bad)
+{
+    if (m < 0 || k <= 0 || k % 32 != 0) return -1;
+    const int64_t nb = k / 32;
+    for (int64_t t = 0; t < m; ++t) {
+        int row_bad = 0;
+        float row_amax = 0.0f;
+        for (int64_t c = 0; c < k; ++c) {
+            const float x = x_at(X, t, c, m, k);
+            if (!isfinite(x)) row_bad = 1;
+            else if (fabsf(x) > row_amax) row_amax = fabsf(x);
+        }
+        bad[t] = row_bad;
+        for (int64_t b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float x = x_at(X, t, 32 * b + i, m, k);
+                if (isfinite(x) && fabsf(x) > amax) amax = fabsf(x);
+            }
+            if (g_mutation == MUT_A8_ROW_SCALE) amax = row_amax;
+            const float top = g_mutation == MUT_A8_SCALE_128 ? 128.0f : 127.0f;
+            scales[t * nb + b] = row_bad ? 0.0f : amax / top;
+            const float inv = amax > 0.0f ? top / amax : 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float v = row_bad ? 0.0f : x_at(X, t, 32 * b + i, m, k) * inv;
+                float r;
+                if (g_mutation == MUT_A8_ROUND_AWAY) r = roundf(v);
+                else if (g_mutation == MUT_A8_TRUNCATE) r = truncf(v);
+                else r = rintf(v);           /* round-half-even (default rounding mode) */
+                codes[t * k + 32 * b + i] = (int8_t)(r > 127.0f ? 127.0f : (r < -127.0f ? -127.0f : r));
+            }
+        }
+    }
+    return 0;
+}
+
+int q4o_matmul_w4a8(const uint8_t *blocks, const float *X, int64_t m, int64_t k, int64_t n,
+                    double *Y, double *B8, int nthreads)
+{
+    if (m < 0 || n <= 0 || k <= 0 || k % 32 != 0) return -1;
+    const int64_t nb = k / 32;
+    int8_t *codes = (int8_t *)malloc((size_t)(m > 0 ? m : 1) * (size_t)k);
+    float *scales = (float *)malloc((size_t)(m > 0 ? m : 1) * (size_t)nb * sizeof(float));
+    int *bad = (int *)malloc((size_t)(m > 0 ? m : 1) * sizeof(int));
+    if (!codes || !scales || !bad) {
+        free(codes);
+        free(scales);
+        free(bad);
+        return -1;
+    }
+    q4o_quantize_x_w4a8(X, m, k, codes, scales, bad);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t j = 0; j < n; ++j) {
+        for (int64_t t = 0; t < m; ++t) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *blk = block_at(blocks, j, b, n, nb);
+                const uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+                const double d = q4o_fp16_to_double(dbits);
+                int64_t dot = 0;
+                for (int i = 0; i < 32; ++i) {
+                    const int q = nibble(blk + 2, i) - (g_mutation == MUT_A8_NO_OFFSET ? 0 : 8);
+                    dot += (int64_t)q * codes[t * k + 32 * b + i];
+                }
+                const double term = d * (double)scales[t * nb + b] * (double)dot;
+                acc += term;
+                mag += fabs(term);
+            }
+            if (Y) Y[t * n + j] = bad[t] ? NAN : acc;
+            if (B8) B8[t * n + j] = bad[t] ? NAN : mag;
+        }
+    }
+    free(codes);
+    free(scales);
+    free(bad);
+    return 0;
 }

@@ -15,7 +15,11 @@ Pins used:
   * a brute-force special case: the product reduces to numpy's matmul of
     the dequantised matrix, which numpy builds from the bytes by itself;
   * invariants: exact power-of-two homogeneity, oddness in X and in d,
-    linearity in X, B >= |Y| with equality for same-sign terms.
+    linearity in X, B >= |Y| with equality for same-sign terms;
+  * for the W4A8 variant: hand-derived codes and products (round-half-even
+    ties, a scale per block), all-eights gives zero, integer-coded X reduces
+    it to the exact product above, power-of-two homogeneity, NaN rows, and
+    the coding error bound against the exact product.
 """
 
 import json
@@ -195,9 +199,101 @@ def pin_sampled_matches_full(orc):
     assert np.array_equal(Ys, Y[t, j]) and np.array_equal(Bs, B[t, j]), "sampled == full"
 
 
+# ---------------------------------------------------------------- W4A8 --
+
+def _w4a8_blocks(k, d_bits, nibble=9):
+    """One row of blocks: the given fp16 scale bits, every nibble the same."""
+    nb = k // 32
+    blocks = np.zeros((1, nb, 18), dtype=np.uint8)
+    for b in range(nb):
+        blocks[0, b, 0] = d_bits[b] & 0xFF
+        blocks[0, b, 1] = d_bits[b] >> 8
+        blocks[0, b, 2:] = nibble | (nibble << 4)
+    return blocks
+
+
+def pin_w4a8_golden(orc):
+    """Hand-derived codes and products (tests/golden/w4a8_blocks.json)."""
+    g = _golden("w4a8_blocks.json")
+    for case in g["cases"]:
+        k = case["k"]
+        X = np.zeros((1, k), dtype=np.float32)
+        for i, v in case["x_nonzero"].items():
+            X[0, int(i)] = v
+        codes, scales, bad = orc.quantize_x_w4a8(X, k)
+        want = np.zeros(k, dtype=np.int8)
+        for i, v in case["codes_nonzero"].items():
+            want[int(i)] = v
+        assert np.array_equal(codes[0], want), f"{case['name']}: codes {codes[0][codes[0] != 0]}"
+        if "scale_block1" in case:
+            assert float(scales[0, 1]) == case["scale_block1"], f"{case['name']}: scale"
+        Y, B = orc.matmul_w4a8(_w4a8_blocks(k, case["d_bits"]), X, 1, k)
+        assert abs(Y[0, 0] - case["y"]) <= 1e-12 * abs(case["y"]), f"{case['name']}: y {Y[0, 0]} != {case['y']}"
+
+
+def pin_w4a8_all_eights_is_zero(orc):
+    """Every nibble 8 means every weight 0, whatever X and d."""
+    k = 96
+    X = synth.activations(3, k, seed=81)
+    Y, B = orc.matmul_w4a8(_w4a8_blocks(k, [0x3C00, 0x4400, 0xB800], nibble=8), X, 1, k)
+    assert np.all(Y == 0.0) and np.all(B == 0.0), "all-eights W4A8 product is zero"
+
+
+def pin_w4a8_integer_case_is_the_exact_product(orc):
+    """Integer X with |x| <= 127 and some |x| = 127 in every block: the codes
+    are X itself and every scale 1, so the W4A8 product is the exact product
+    (pinned above); power-of-two d keeps every sum exact in fp64."""
+    rng = np.random.default_rng(83)
+    n, k, m = 9, 160, 4
+    blocks = synth.q4_0_blocks(n, k, seed=84).reshape(n, k // 32, 18).copy()
+    e = rng.integers(-6, 3, size=(n, k // 32))
+    dbits = (2.0 ** e).astype(np.float16) * np.where(rng.random((n, k // 32)) < 0.5, -1, 1).astype(np.float16)
+    raw = dbits.view(np.uint16)
+    blocks[:, :, 0] = raw & 0xFF
+    blocks[:, :, 1] = raw >> 8
+    X = rng.integers(-126, 127, size=(m, k)).astype(np.float32)
+    X[:, ::32] = np.where(rng.random((m, k // 32)) < 0.5, -127.0, 127.0)
+    Y8, B8 = orc.matmul_w4a8(blocks, X, n, k)
+    Y, B = orc.matmul(blocks, X, n, k)
+    assert np.array_equal(Y8, Y), "integer-coded X: W4A8 equals the exact product"
+
+
+def pin_w4a8_homogeneity_and_nan(orc):
+    """X * 2^p scales every code's scale by 2^p and leaves the codes: Y * 2^p
+    exactly. A row holding a NaN gives NaN outputs; other rows are unchanged."""
+    n, k, m = 11, 128, 3
+    blocks = synth.q4_0_blocks(n, k, seed=85)
+    X = synth.activations(m, k, seed=86)
+    Y, _ = orc.matmul_w4a8(blocks, X, n, k)
+    Y2, _ = orc.matmul_w4a8(blocks, X * np.float32(8.0), n, k)
+    assert np.array_equal(Y2, Y * 8.0), "W4A8 homogeneity"
+    Xn = X.copy()
+    Xn[1, 70] = np.nan
+    Yn, _ = orc.matmul_w4a8(blocks, Xn, n, k)
+    assert np.all(np.isnan(Yn[1])) and np.array_equal(Yn[[0, 2]], Y[[0, 2]]), "W4A8 NaN row"
+
+
+def pin_w4a8_quantization_bound(orc):
+    """|Y8 - Y| <= sum_b |d| * s_b / 2 * sum_i |q - 8| (each code within half a
+    step of x / s), with a little slack for fp64 rounding."""
+    n, k, m = 13, 256, 3
+    blocks = synth.q4_0_blocks(n, k, seed=87)
+    X = synth.activations(m, k, seed=88)
+    Y8, _ = orc.matmul_w4a8(blocks, X, n, k)
+    Y, _ = orc.matmul(blocks, X, n, k)
+    codes, scales, bad = orc.quantize_x_w4a8(X, k)
+    W = orc.dequant_matrix(blocks, n, k)                       # (q - 8) * d, [n x k]
+    bound = np.zeros((m, n))
+    for b in range(k // 32):
+        Wb = np.abs(W[:, 32 * b:32 * b + 32]).sum(axis=1)     # |d| * sum |q - 8|
+        bound += np.outer(scales[:, b].astype(np.float64) / 2, Wb)
+    assert np.all(np.abs(Y8 - Y) <= bound * (1 + 1e-9) + 1e-12), "W4A8 within the coding bound"
+
+
 PINS = [pin_golden_block, pin_format_facts, pin_all_eights_is_zero, pin_nibble_order,
         pin_fp16_exhaustive, pin_exact_integer, pin_numpy_special_case, pin_invariants,
-        pin_sampled_matches_full]
+        pin_sampled_matches_full, pin_w4a8_golden, pin_w4a8_all_eights_is_zero,
+        pin_w4a8_integer_case_is_the_exact_product, pin_w4a8_homogeneity_and_nan, pin_w4a8_quantization_bound]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
