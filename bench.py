@@ -65,6 +65,10 @@ SWEEP = [
     dict(name="slot sweep 14336x4096", m=16, n=14336, k=4096),
     dict(name="logit head", m=4, n=151936, k=2560),
     dict(name="prefill", m=540, n=9728, k=2560),
+    # the integer-dot variant (q4_0_matmul_w4a8): X coded to int8 per block
+    dict(name="W4A8 decode up-projection", m=1, n=9728, k=2560, w4a8=True),
+    dict(name="W4A8 slot sweep 14336x4096", m=8, n=14336, k=4096, w4a8=True),
+    dict(name="W4A8 slot sweep 14336x4096", m=16, n=14336, k=4096, w4a8=True),
 ]
 
 
@@ -197,10 +201,11 @@ class ClockSampler:
 class Workload:
     """Packed weight copies, X and Y resident on the GPU for one shape."""
 
-    def __init__(self, q4lib, m, n, k, min_copies=1):
+    def __init__(self, q4lib, m, n, k, min_copies=1, w4a8=False):
         import torch
         from q4_quantized_linear_gb300 import synth
         self.m, self.n, self.k = m, n, k
+        self.w4a8 = w4a8
         self.blocks = synth.q4_0_blocks(n, k, seed=0)
         self.X = synth.activations(m, k, seed=0)
         wb = weight_bytes(n, k)
@@ -216,6 +221,9 @@ class Workload:
         torch.cuda.synchronize()
 
     def step(self, q4lib, i, stream):
+        if self.w4a8:
+            q4lib.q4_0_matmul_w4a8(self.W[i % self.copies], self.Xd, self.Yd, self.m, self.k, self.n, stream)
+            return
         q4lib.q4_0_matmul_ws(self.W[i % self.copies], self.Xd, self.Yd, self.m, self.k, self.n,
                              self.ws, self.wsb, stream)
 
@@ -318,7 +326,7 @@ def run_sweep(q4lib, stream, peaks):
     out = []
     for cfg in SWEEP:
         m, n, k = cfg["m"], cfg["n"], cfg["k"]
-        wl = Workload(q4lib, m, n, k)
+        wl = Workload(q4lib, m, n, k, w4a8=cfg.get("w4a8", False))
         wb = weight_bytes(n, k)
         est = wb / (peaks["hbm_gbs"] * 1e9) if m <= 16 else 2.0 * m * n * k / (peaks["bf16_tflops"] * 1e12)
         steps = int(min(20000, max(200, 0.25 / max(est, 1e-7))))

@@ -148,6 +148,30 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
                             int64_t m, int64_t k, int64_t n,
                             void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
 
+/* W4A8: Y[m x n] = X[m x k] . W^T with X coded to int8 first, so that every
+ * block's dot product is an integer one. The pages name the integer dot
+ * product (goinfer ch. 10, "Which kernel runs is a runtime decision": the
+ * canonical quantized dot of integer-dot hardware; rembed "Architecture",
+ * "int8 quantization": activations quantised, integer products bit-exact
+ * against an integer reference) but print no coding rule; the one used:
+ * per 32-element block of an X row, amax = max |x|, scale s = amax / 127 and
+ * code c = round-half-even(x * (127 / amax)), all in fp32 (one IEEE quotient
+ * or product each), so |c| <= 127; a block with amax = 0 has codes 0 and
+ * s = 0. Then Y[t][j] = sum_b d(j,b) * s(t,b) * sum_i (q - 8) * c: each block's
+ * integer sum is exact (fp16 operands, fp32 accumulation of integers below
+ * 2^24), d * s and the sum over blocks are fp32, so |Y - Y_w4a8| <= 4e-5 * B8
+ * + 1e-6 against the fp64 value, B8 = sum_b |d s sum_i (q - 8) c|. A row of X
+ * holding a NaN or an infinity gives NaN in every output of that row.
+ *   W_packed: device, packed by q4_0_pack for (n, k), 16-byte aligned.
+ *   X: device fp32 [m x k] row-major, 16-byte aligned; Y: device fp32
+ *   [m x n] row-major, overwritten, 4-byte aligned.
+ *   0 <= m <= 16 (m == 0 does nothing; larger m is refused with
+ *   Q4_ERR_INVALID_ARG), n >= 1, k >= 32, k % 32 == 0.
+ * Runs in the whole-record decode kernel, eight tokens per MMA column tile;
+ * needs no scratch and allocates nothing. */
+Q4MM_API int q4_0_matmul_w4a8(const void *W_packed, const float *X, float *Y,
+                              int64_t m, int64_t k, int64_t n, q4mm_stream_t stream);
+
 /* Size of the library's fixed scratch array used by q4_0_matmul_static_scratch. */
 #define Q4_STATIC_SCRATCH_BYTES (8u << 20)
 

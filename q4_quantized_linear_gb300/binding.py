@@ -38,6 +38,7 @@ _SIGS = {
     "q4_0_matmul_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "q4_0_matmul": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_ws": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
+    "q4_0_matmul_w4a8": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_static_scratch": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots_ws": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -129,6 +130,11 @@ def q4_0_unpack(blocks, W_packed, n: int, k: int, stream=None, check: bool = Tru
 def q4_0_matmul(W_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:
     rc = _lib.q4_0_matmul(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _stream(stream))
     return _check(rc, "q4_0_matmul") if check else rc
+
+
+def q4_0_matmul_w4a8(W_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_0_matmul_w4a8(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _stream(stream))
+    return _check(rc, "q4_0_matmul_w4a8") if check else rc
 
 
 def q4_0_matmul_ws(W_packed, X, Y, m: int, k: int, n: int, workspace, workspace_bytes: int,

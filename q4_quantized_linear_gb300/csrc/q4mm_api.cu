@@ -199,7 +199,7 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         if (kind == Q4_DECODE_CUDA_CORE || kind == Q4_DECODE_RECORD_MMA) {
             GemvPlan gp;
             if (!plan_gemv(m, k, n, dev.sm_count, &gp)) return Q4_ERR_INVALID_ARG;
-            return map_cuda(launch_gemv(gp, a, kind == Q4_DECODE_RECORD_MMA, s));
+            return map_cuda(launch_gemv(gp, a, kind == Q4_DECODE_RECORD_MMA ? kGemvModeRecordMma : kGemvModeFma, s));
         }
         DecodePlan plan;
         if (!plan_decode(m, k, n, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
@@ -350,6 +350,36 @@ Q4MM_API int q4_0_matmul(const void *W_packed, const float *X, float *Y, int64_t
 {
     return matmul_impl(W_packed, X, k, nullptr, Y, n, m, k, n, nullptr, 0, true,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+Q4MM_API int q4_0_matmul_w4a8(const void *W_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,
+                              q4mm_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!W_packed || !X || !Y || m < 0 || m > kRecordMmaMaxM || !valid_nk(n, k)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W_packed, 16) || !aligned(X, 16) || !aligned(Y, 4)) return Q4_ERR_ALIGNMENT;
+    if (m == 0) return Q4_OK;
+    DeviceInfo dev;
+    int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    DecodeArgs a{};
+    a.W = static_cast<const uint8_t *>(W_packed);
+    a.X = X;
+    a.rows = nullptr;
+    a.ldx = k;
+    a.Y = Y;
+    a.ldy = n;
+    a.status = dev.status;
+    a.wait_ns = g_wait_ns.load();
+    a.m = static_cast<int>(m);
+    a.n = static_cast<int>(n);
+    a.nb = static_cast<int>(k / 32);
+    a.np = static_cast<int>(ceil_div(k, kPairK));
+    a.groups = static_cast<int>(ceil_div(n, kGroupRows));
+    a.prefetch_w = g_prefetch_w.load();
+    GemvPlan gp;
+    if (!plan_gemv(m, k, n, dev.sm_count, &gp)) return Q4_ERR_INVALID_ARG;
+    return map_cuda(launch_gemv(gp, a, kGemvModeW4A8, s));
 }
 
 Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,

@@ -268,7 +268,7 @@ __device__ __forceinline__ void x_load(const float *xrow, int blk, bool live, in
 // agree on the scale.
 __device__ __forceinline__ void x_fragments(const float4 &xa, const float4 &xb, int lane, uint4 &bf, float &inv)
 {
-    const int g = lane >> 2, t = lane & 3, h = g & 1;
+    const int h = (lane >> 2) & 1;
     unsigned mb = max(absmax_bits(xa), absmax_bits(xb));
     mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
     mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
@@ -325,6 +325,87 @@ __device__ __forceinline__ void mma_record(const uint8_t *rec, const uint4 bf[NT
                 mma_f16(D, A[b][1], bf[nt][b].z, bf[nt][b].w, D);
                 y[nt][rt][0] = fmaf((b ? d0.y : d0.x) * su[nt][b], D[0] + D[1], y[nt][rt][0]);
                 y[nt][rt][1] = fmaf((b ? d1.y : d1.x) * su[nt][b], D[2] + D[3], y[nt][rt][1]);
+            }
+    }
+}
+
+// ------------------------------------------------------------------------
+// W4A8 mode (the integer-dot variant, q4_0_matmul_w4a8): X is coded per
+// 32-element block to int8, c = round-half-even(x * (127 / amax)), scale
+// s = amax / 127, both in fp32 exactly as written (IEEE quotient and
+// product); a block with amax = 0 has codes 0 and scale 0, and a block holding
+// a NaN or an infinity gets a NaN scale, which makes every output of its row
+// NaN. The codes and (q - 8) are exact in fp16 and a block's integer dot
+// product (at most 32 * 8 * 127 in size) is exact in the MMA's fp32
+// accumulator, so each block's dot is the integer one; d * s is applied to it
+// in fp32. Column g of the eight MMA columns is token g of the column tile.
+
+// This lane's B fragment of one block (the codes of its column's token,
+// elements 4t .. 4t + 3 and 16 + 4t .. 19 + 4t, in the K permutation of the
+// hi/lo mode) and the block's scale s for that token. Lanes 4g .. 4g + 3
+// agree on amax.
+__device__ __forceinline__ void x_codes(const float4 &xa, const float4 &xb, uint4 &bf, float &scale)
+{
+    unsigned mb = max(absmax_bits(xa), absmax_bits(xb));
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+    const float amax = __uint_as_float(mb);
+    const bool finite = mb < 0x7F800000u;
+    const float inv = (finite && mb != 0u) ? __fdiv_rn(127.0f, amax) : 0.0f;
+    scale = finite ? __fdiv_rn(amax, 127.0f) : __uint_as_float(0x7FC00000u);
+    auto code2 = [inv](float lo, float hi) {
+        const __half2 h = __halves2half2(__int2half_rn(__float2int_rn(__fmul_rn(lo, inv))),
+                                         __int2half_rn(__float2int_rn(__fmul_rn(hi, inv))));
+        return *reinterpret_cast<const uint32_t *>(&h);
+    };
+    bf.x = code2(xa.x, xa.z);   // k-step 0: elements 4t, 4t+2
+    bf.y = code2(xb.x, xb.z);   //           16+4t, 18+4t
+    bf.z = code2(xa.y, xa.w);   // k-step 1: 4t+1, 4t+3
+    bf.w = code2(xb.y, xb.w);   //           17+4t, 19+4t
+}
+
+// One record through the tensor core in W4A8 mode: y[nt][rt][0..3] += rows
+// 16 rt + g (0, 1) and 16 rt + g + 8 (2, 3), tokens 8 nt + 2t (0, 2) and
+// 8 nt + 2t + 1 (1, 3). sc[nt][b][0 / 1]: the block's scales of those two
+// tokens.
+template <int NT>
+__device__ __forceinline__ void mma_record_a8(const uint8_t *rec, const uint4 bf[NT][2], const float sc[NT][2][2],
+                                              int lane, float y[NT][8][4])
+{
+    const int g = lane >> 2, t = lane & 3;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t base = smem_u32(rec);
+#pragma unroll
+    for (int rt = 0; rt < 8; ++rt) {
+        const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
+        uint32_t sc0, sc1, q00, q01, q10, q11;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc0) : "r"(base + kRecScaleOff + 4 * r0));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc1) : "r"(base + kRecScaleOff + 4 * r0 + 32));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q00) : "r"(base + kRecQs0Off + 16 * r0 + 4 * t));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q01) : "r"(base + kRecQs0Off + 16 * r0 + 4 * t + 128));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q10) : "r"(base + kRecQs1Off + 16 * r0 + 4 * t));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(q11) : "r"(base + kRecQs1Off + 16 * r0 + 4 * t + 128));
+        uint32_t v00[4], v01[4], v10[4], v11[4];
+        unpack_word_f16(q00, v00);
+        unpack_word_f16(q01, v01);
+        unpack_word_f16(q10, v10);
+        unpack_word_f16(q11, v11);
+        const uint32_t A[2][2][4] = {{{v00[0], v01[0], v00[1], v01[1]}, {v00[2], v01[2], v00[3], v01[3]}},
+                                     {{v10[0], v11[0], v10[1], v11[1]}, {v10[2], v11[2], v10[3], v11[3]}}};
+        const float2 d0 = __half22float2(*reinterpret_cast<const __half2 *>(&sc0));   // row g: block 0, 1
+        const float2 d1 = __half22float2(*reinterpret_cast<const __half2 *>(&sc1));   // row g + 8
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float D[4];
+                mma_f16(D, A[b][0], bf[nt][b].x, bf[nt][b].y, zero4);
+                mma_f16(D, A[b][1], bf[nt][b].z, bf[nt][b].w, D);
+                const float dg = b ? d0.y : d0.x, dg8 = b ? d1.y : d1.x;
+                y[nt][rt][0] = fmaf(__fmul_rn(dg, sc[nt][b][0]), D[0], y[nt][rt][0]);
+                y[nt][rt][1] = fmaf(__fmul_rn(dg, sc[nt][b][1]), D[1], y[nt][rt][1]);
+                y[nt][rt][2] = fmaf(__fmul_rn(dg8, sc[nt][b][0]), D[2], y[nt][rt][2]);
+                y[nt][rt][3] = fmaf(__fmul_rn(dg8, sc[nt][b][1]), D[3], y[nt][rt][3]);
             }
     }
 }
@@ -425,7 +506,7 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const GSmem &s
     return true;
 }
 
-template <int M, bool MMA>
+template <int M, bool MMA, bool A8>
 __global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -498,8 +579,9 @@ __global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const Dec
     // 16-31 block 2p + 1 for the same columns, handed to lanes 0-15 by
     // shuffles. With one column tile a warp's X values are loaded one record
     // ahead; with more (m = 5..16) they are loaded where they are used (L1).
-    constexpr int NT = MMA ? (M + 3) / 4 : 1;
-    constexpr bool kOnePass = MMA && M <= 2;
+    // (W4A8 mode: column tile nt holds tokens 8 nt .. 8 nt + 7, one per column)
+    constexpr int NT = A8 ? (M + 7) / 8 : (MMA ? (M + 3) / 4 : 1);
+    constexpr bool kOnePass = MMA && !A8 && M <= 2;
     const int xb1 = kOnePass ? (lane >> 4) : 0;       // block of the pair this lane builds
     const int col_tok = kOnePass ? ((lane & 15) >> 3) : (lane >> 3);
     const bool col_live = col_tok < M && col_tok < a.m;
@@ -509,10 +591,11 @@ __global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const Dec
     bool livet[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const int tok = 4 * nt + (lane >> 3);
-        livet[nt] = nt > 0 ? (tok < M && tok < a.m) : col_live;
-        xcolt[nt] = nt > 0 ? a.X + (livet[nt] ? static_cast<int64_t>(a.rows ? __ldg(a.rows + tok) : tok) * a.ldx : 0)
-                           : xcol;
+        const int tok = A8 ? 8 * nt + (lane >> 2) : 4 * nt + (lane >> 3);
+        const bool own = A8 || nt > 0;
+        livet[nt] = own ? (tok < M && tok < a.m) : col_live;
+        xcolt[nt] = own ? a.X + (livet[nt] ? static_cast<int64_t>(a.rows ? __ldg(a.rows + tok) : tok) * a.ldx : 0)
+                        : xcol;
     }
 
     bool ok = true;
@@ -522,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const Dec
     // record-MMA mode: X values of the warp's next record, loaded one record
     // ahead so that their latency hides behind the current record's work
     float4 xn[2][2];
-    if (MMA && NT == 1 && ci < ntiles) {
+    if (MMA && !A8 && NT == 1 && ci < ntiles) {
         const int b0 = 2 * (p0 + cj);
         if (kOnePass) {
             x_load(xcol, b0 + xb1, col_live && b0 + xb1 < a.nb, lane, xn[0][0], xn[0][1]);
@@ -539,15 +622,36 @@ __global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const Dec
 #pragma unroll
             for (int t = 0; t < M; ++t) yp[r][t] = 0.0f;
         float yq[NT][8][2];
+        float y8[NT][8][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int r = 0; r < 8; ++r) yq[nt][r][0] = yq[nt][r][1] = 0.0f;
+            for (int r = 0; r < 8; ++r) {
+                yq[nt][r][0] = yq[nt][r][1] = 0.0f;
+                y8[nt][r][0] = y8[nt][r][1] = y8[nt][r][2] = y8[nt][r][3] = 0.0f;
+            }
         for (; ci == g; step_pos(ci, cj, P)) {
             if (!warp_wait(&sm.full_w[s], ph, a.wait_ns)) { ok = false; break; }
             const uint8_t *rec = sm.w + static_cast<size_t>(s) * kRecordBytes;
             const int b0 = 2 * (p0 + cj);
-            if (MMA) {
+            if constexpr (A8) {
+                // a missing second block is padding (weights exactly 0) against X = 0
+                uint4 bf[NT][2];
+                float sc[NT][2][2];
+                const int tq = lane & 3;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        float4 xa, xb;
+                        x_load(xcolt[nt], b0 + b, livet[nt] && b0 + b < a.nb, lane, xa, xb);
+                        float scale;
+                        x_codes(xa, xb, bf[nt][b], scale);
+                        sc[nt][b][0] = __shfl_sync(0xFFFFFFFFu, scale, 8 * tq);       // token 2 tq's column
+                        sc[nt][b][1] = __shfl_sync(0xFFFFFFFFu, scale, 8 * tq + 4);   // token 2 tq + 1
+                    }
+                mma_record_a8<NT>(rec, bf, sc, lane, y8);
+            } else if (MMA) {
                 // a missing second block is padding (weights exactly 0) against X = 0
                 uint4 bf[NT][2];
                 float su[NT][2];
@@ -615,7 +719,21 @@ __global__ void __launch_bounds__(kThreads, M > 8 ? 1 : 2) gemv_kernel(const Dec
         if (!ok) break;
         if (g >= 2 && !warp_wait(&sm.gfree[tb], ((g >> 1) & 1) ^ 1u, a.wait_ns)) { ok = false; break; }
         float *pp = sm.part + (tb * kWarps + c) * M * kGroupRows;
-        if (MMA) {
+        if constexpr (A8) {
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int tok = 8 * nt + 2 * t + c2;
+                    if (tok < M)
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            pp[tok * kGroupRows + 16 * r + g] = y8[nt][r][c2];
+                            pp[tok * kGroupRows + 16 * r + g + 8] = y8[nt][r][2 + c2];
+                        }
+                }
+        } else if (MMA) {
             const int g = lane >> 2;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -672,35 +790,40 @@ size_t gemv_smem(int M, int S, int ring)
     return static_cast<size_t>(ring) * kRecordBytes + part + red + bars;
 }
 
-const void *gemv_fn(int M, bool mma)
-{
-    if (mma) {
-        switch (M) {
-        case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, true>);
-        case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, true>);
-        case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, true>);
-        case 4: return reinterpret_cast<const void *>(&gemv_kernel<4, true>);
-        case 5: return reinterpret_cast<const void *>(&gemv_kernel<5, true>);
-        case 6: return reinterpret_cast<const void *>(&gemv_kernel<6, true>);
-        case 7: return reinterpret_cast<const void *>(&gemv_kernel<7, true>);
-        case 8: return reinterpret_cast<const void *>(&gemv_kernel<8, true>);
-        case 9: return reinterpret_cast<const void *>(&gemv_kernel<9, true>);
-        case 10: return reinterpret_cast<const void *>(&gemv_kernel<10, true>);
-        case 11: return reinterpret_cast<const void *>(&gemv_kernel<11, true>);
-        case 12: return reinterpret_cast<const void *>(&gemv_kernel<12, true>);
-        case 13: return reinterpret_cast<const void *>(&gemv_kernel<13, true>);
-        case 14: return reinterpret_cast<const void *>(&gemv_kernel<14, true>);
-        case 15: return reinterpret_cast<const void *>(&gemv_kernel<15, true>);
-        default: return reinterpret_cast<const void *>(&gemv_kernel<16, true>);
-        }
+#define Q4_GEMV_CASES(MMA, A8)                                                                  \
+    switch (M) {                                                                               \
+    case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, MMA, A8>);                   \
+    case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, MMA, A8>);                   \
+    case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, MMA, A8>);                   \
+    case 4: return reinterpret_cast<const void *>(&gemv_kernel<4, MMA, A8>);                   \
+    case 5: return reinterpret_cast<const void *>(&gemv_kernel<5, MMA, A8>);                   \
+    case 6: return reinterpret_cast<const void *>(&gemv_kernel<6, MMA, A8>);                   \
+    case 7: return reinterpret_cast<const void *>(&gemv_kernel<7, MMA, A8>);                   \
+    case 8: return reinterpret_cast<const void *>(&gemv_kernel<8, MMA, A8>);                   \
+    case 9: return reinterpret_cast<const void *>(&gemv_kernel<9, MMA, A8>);                   \
+    case 10: return reinterpret_cast<const void *>(&gemv_kernel<10, MMA, A8>);                 \
+    case 11: return reinterpret_cast<const void *>(&gemv_kernel<11, MMA, A8>);                 \
+    case 12: return reinterpret_cast<const void *>(&gemv_kernel<12, MMA, A8>);                 \
+    case 13: return reinterpret_cast<const void *>(&gemv_kernel<13, MMA, A8>);                 \
+    case 14: return reinterpret_cast<const void *>(&gemv_kernel<14, MMA, A8>);                 \
+    case 15: return reinterpret_cast<const void *>(&gemv_kernel<15, MMA, A8>);                 \
+    default: return reinterpret_cast<const void *>(&gemv_kernel<16, MMA, A8>);                 \
     }
+
+// The kernel instance for M tokens in a mode (the CUDA-core mode is built for
+// M <= 4 only).
+const void *gemv_fn(int M, int mode)
+{
+    if (mode == kGemvModeW4A8) Q4_GEMV_CASES(true, true)
+    if (mode == kGemvModeRecordMma) Q4_GEMV_CASES(true, false)
     switch (M) {
-    case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, false>);
-    case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, false>);
-    case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, false>);
-    default: return reinterpret_cast<const void *>(&gemv_kernel<4, false>);
+    case 1: return reinterpret_cast<const void *>(&gemv_kernel<1, false, false>);
+    case 2: return reinterpret_cast<const void *>(&gemv_kernel<2, false, false>);
+    case 3: return reinterpret_cast<const void *>(&gemv_kernel<3, false, false>);
+    default: return reinterpret_cast<const void *>(&gemv_kernel<4, false, false>);
     }
 }
+#undef Q4_GEMV_CASES
 
 // Largest number of clusters of S CTAs of the M-token kernel with `smem`
 // bytes of dynamic shared memory that the current device can hold at once
@@ -719,7 +842,7 @@ int max_active_clusters(int M, int S, size_t smem)
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void *fn = gemv_fn(M, M > kGemvMaxM);        // the CUDA-core mode is built for m <= 4 only
+    const void *fn = gemv_fn(M, M > kGemvMaxM ? kGemvModeRecordMma : kGemvModeFma);
     int n = 0;
     if (set_max_smem(fn, smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
@@ -822,9 +945,9 @@ bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan)
     return true;
 }
 
-cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, bool mma, cudaStream_t s)
+cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, int mode, cudaStream_t s)
 {
-    const void *fn = gemv_fn(plan.M, mma);
+    const void *fn = gemv_fn(plan.M, mode);
     cudaError_t e = set_max_smem(fn, plan.smem);
     if (e != cudaSuccess) return e;
     DecodeArgs a = args;

@@ -116,9 +116,11 @@ struct GemvPlan {
 };
 
 bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan);
-// mma: the record-MMA mode (exact fp16 (q - 8) on the warp-level tensor core)
-// instead of fp32 FMAs; the same plan serves both.
-cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, bool mma, cudaStream_t s);
+// Modes of the kernel; the same plan serves all three.
+constexpr int kGemvModeFma = 0;         // fp32 FMAs on the CUDA cores (m <= 4)
+constexpr int kGemvModeRecordMma = 1;   // exact fp16 (q - 8) times X split into fp16 hi + lo, mma.sync
+constexpr int kGemvModeW4A8 = 2;        // X coded to int8 per block, integer block dots on mma.sync
+cudaError_t launch_gemv(const GemvPlan &plan, const DecodeArgs &args, int mode, cudaStream_t s);
 
 // ------------------------------------------------------------ warp MMA --
 

@@ -62,6 +62,17 @@ def test_matmul_rejects_bad_arguments_on_the_host(q4lib, args, code):
     assert q4lib.q4_0_matmul(*args, stream=0, check=False) == code
 
 
+@pytest.mark.parametrize("args,code", [
+    ((0, 0x1000, 0x1000, 1, 64, 64), 1),        # null W
+    ((0x1000, 0x1000, 0x1000, 17, 64, 64), 1),  # m > 16
+    ((0x1000, 0x1000, 0x1000, -1, 64, 64), 1),  # m < 0
+    ((0x1000, 0x1000, 0x1000, 1, 48, 64), 1),   # k % 32 != 0
+    ((0x1000, 0x1004, 0x1000, 1, 64, 64), 2),   # X not 16-byte aligned
+])
+def test_w4a8_rejects_bad_arguments_on_the_host(q4lib, args, code):
+    assert q4lib.q4_0_matmul_w4a8(*args, stream=0, check=False) == code
+
+
 def test_batched_slots_rejects_bad_leading_dimensions(q4lib):
     # ldx < k, ldx % 4 != 0, ldy < n, null slot ids
     assert q4lib.q4_0_matmul_batched_slots(0x1000, 0x1000, 32, 0x1000, 2, 0x1000, 64, 64, 64,
