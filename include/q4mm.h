@@ -66,6 +66,8 @@ typedef struct CUstream_st *q4mm_stream_t;
 #define Q4_ERR_DEVICE_TIMEOUT 5     /* a kernel's bounded wait ran out (read by q4_last_device_status) */
 #define Q4_ERR_WORKSPACE 6          /* workspace missing or smaller than q4_0_matmul_workspace_size() */
 #define Q4_ERR_NO_MEMORY 7          /* the library could not allocate its own workspace */
+#define Q4_ERR_IO 8                 /* a file could not be opened or read */
+#define Q4_ERR_FORMAT 9             /* a file breaks the GGUF layout (q4_gguf_open) */
 
 /*
  * Packed weight layout (what q4_0_pack writes). Repacking the blocks at load
@@ -280,6 +282,47 @@ Q4MM_API int q4_debug_set_trace(void *buffer, size_t bytes, uint32_t cta);
  * barrier nothing ever completes, for at most limit_ns nanoseconds, then
  * records Q4_ERR_DEVICE_TIMEOUT in the device status word and returns. */
 Q4MM_API int q4_selftest_wait_timeout(uint64_t limit_ns, q4mm_stream_t stream);
+
+/* ------------------------------------------------------------- GGUF --
+ * A reader of GGUF files in front of q4_0_pack (host code, no device work).
+ * "Go AI Inference: What is Inference?", section "GGUF: The Whole Model in
+ * One File": a header (magic GGUF, version, tensor and metadata counts),
+ * typed key-value metadata, tensor descriptors (name, shape, type, offset)
+ * and the data blob; section "The blob: getting the weights into memory":
+ * the loader parses the header, metadata and descriptors first, then places
+ * each tensor's bytes. Field widths and type codes follow GGUF versions 2
+ * and 3 as ggml writes them (little endian). A Q4_0 tensor (type 2) of
+ * shape (k, n) (innermost first) holds the [n][k/32] 18-byte blocks that
+ * q4_0_pack takes: read it with q4_gguf_read_tensor, copy it to the device,
+ * pack it once. */
+typedef struct q4_gguf q4_gguf;
+
+/* Parse a file's header, metadata and tensor descriptors; no tensor data is
+ * read. Every size is checked against the file: a file that breaks the
+ * layout (bad magic, version other than 2 or 3, a string, array or tensor
+ * reaching past the end, a descriptor offset not a multiple of
+ * general.alignment) gives Q4_ERR_FORMAT; a file that cannot be read,
+ * Q4_ERR_IO. On success *out owns the parsed file; release it with
+ * q4_gguf_close. */
+Q4MM_API int q4_gguf_open(const char *path, q4_gguf **out);
+Q4MM_API void q4_gguf_close(q4_gguf *g);
+/* Number of tensor descriptors (-1 for a null handle). */
+Q4MM_API int64_t q4_gguf_tensor_count(const q4_gguf *g);
+/* Index of the tensor called `name`, or -1. */
+Q4MM_API int64_t q4_gguf_find_tensor(const q4_gguf *g, const char *name);
+/* Descriptor of tensor `index`: name (owned by g), type, number of dims,
+ * dims[4] (innermost first, unused ones 1), absolute byte offset of its data
+ * in the file and its byte size (0 when the type's size is not one this
+ * reader knows: f32, f16, Q4_0, Q8_0). Any output pointer may be NULL. */
+Q4MM_API int q4_gguf_tensor_info(const q4_gguf *g, int64_t index, const char **name, int *type,
+                                 int *n_dims, int64_t *dims, uint64_t *file_offset, uint64_t *bytes);
+/* Read tensor `index`'s bytes into host memory of at least its byte size
+ * (Q4_ERR_INVALID_ARG if smaller, or if the size is unknown). */
+Q4MM_API int q4_gguf_read_tensor(const q4_gguf *g, int64_t index, void *host_dst, uint64_t dst_bytes);
+/* A metadata value by key: an integer or bool scalar, or a string (owned by
+ * g). Q4_ERR_INVALID_ARG when the key is absent or of another type. */
+Q4MM_API int q4_gguf_get_int(const q4_gguf *g, const char *key, int64_t *value);
+Q4MM_API int q4_gguf_get_string(const q4_gguf *g, const char *key, const char **value);
 
 #ifdef __cplusplus
 }

@@ -49,6 +49,16 @@ _SIGS = {
     "q4_set_decode_kernel": (_INT, [_INT]),
     "q4_selftest_wait_timeout": (_INT, [ctypes.c_uint64, _P]),
     "q4_debug_set_trace": (_INT, [_P, _SZ, ctypes.c_uint32]),
+    "q4_gguf_open": (_INT, [ctypes.c_char_p, ctypes.POINTER(_P)]),
+    "q4_gguf_close": (None, [_P]),
+    "q4_gguf_tensor_count": (_I64, [_P]),
+    "q4_gguf_find_tensor": (_I64, [_P, ctypes.c_char_p]),
+    "q4_gguf_tensor_info": (_INT, [_P, _I64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_INT),
+                                   ctypes.POINTER(_INT), ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_uint64),
+                                   ctypes.POINTER(ctypes.c_uint64)]),
+    "q4_gguf_read_tensor": (_INT, [_P, _I64, _P, ctypes.c_uint64]),
+    "q4_gguf_get_int": (_INT, [_P, ctypes.c_char_p, ctypes.POINTER(_I64)]),
+    "q4_gguf_get_string": (_INT, [_P, ctypes.c_char_p, ctypes.POINTER(ctypes.c_char_p)]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -63,6 +73,9 @@ Q4_ERR_CUDA = 4
 Q4_ERR_DEVICE_TIMEOUT = 5
 Q4_ERR_WORKSPACE = 6
 Q4_ERR_NO_MEMORY = 7
+Q4_ERR_IO = 8
+Q4_ERR_FORMAT = 9
+GGUF_TYPE_Q4_0 = 2
 
 
 class Q4Error(RuntimeError):
@@ -240,3 +253,88 @@ def matmul(W_packed, X, n: int, out=None, stream=None):
     ws, wsb = workspace_for(m, k, n, X.device, stream)
     q4_0_matmul_ws(W_packed, X, Y, m, k, n, ws, wsb, stream)
     return Y
+
+
+# ------------------------------------------------------------------ GGUF --
+
+def q4_gguf_open(path: str) -> int:
+    """Parse a GGUF file's header, metadata and descriptors; returns a handle."""
+    h = _P()
+    _check(_lib.q4_gguf_open(os.fsencode(path), ctypes.byref(h)), "q4_gguf_open")
+    return h.value
+
+
+def q4_gguf_close(handle: int) -> None:
+    _lib.q4_gguf_close(handle)
+
+
+def q4_gguf_tensor_count(handle: int) -> int:
+    return _lib.q4_gguf_tensor_count(handle)
+
+
+def q4_gguf_find_tensor(handle: int, name: str) -> int:
+    return _lib.q4_gguf_find_tensor(handle, name.encode())
+
+
+def q4_gguf_tensor_info(handle: int, index: int) -> dict:
+    name = ctypes.c_char_p()
+    typ, nd = _INT(), _INT()
+    dims = (_I64 * 4)()
+    off, nbytes = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(_lib.q4_gguf_tensor_info(handle, index, ctypes.byref(name), ctypes.byref(typ), ctypes.byref(nd), dims,
+                                    ctypes.byref(off), ctypes.byref(nbytes)), "q4_gguf_tensor_info")
+    return dict(name=name.value.decode(), type=typ.value, dims=list(dims[:nd.value]),
+                file_offset=off.value, bytes=nbytes.value)
+
+
+def q4_gguf_read_tensor(handle: int, index: int, host_dst, dst_bytes: int, check: bool = True) -> int:
+    rc = _lib.q4_gguf_read_tensor(handle, index, _addr_host(host_dst), dst_bytes)
+    return _check(rc, "q4_gguf_read_tensor") if check else rc
+
+
+def q4_gguf_get_int(handle: int, key: str) -> int:
+    v = _I64()
+    _check(_lib.q4_gguf_get_int(handle, key.encode(), ctypes.byref(v)), "q4_gguf_get_int")
+    return v.value
+
+
+def q4_gguf_get_string(handle: int, key: str) -> str:
+    v = ctypes.c_char_p()
+    _check(_lib.q4_gguf_get_string(handle, key.encode(), ctypes.byref(v)), "q4_gguf_get_string")
+    return v.value.decode()
+
+
+def _addr_host(a) -> int:
+    """Host address of a contiguous numpy array."""
+    return a.ctypes.data
+
+
+def gguf_q4_0_blocks(path: str, name: str):
+    """(blocks, n, k): a Q4_0 tensor's [n][k/32] 18-byte blocks, read from a
+    GGUF file into a host numpy array (uint8, shape (n, k/32, 18))."""
+    import numpy as np
+    h = q4_gguf_open(path)
+    try:
+        i = q4_gguf_find_tensor(h, name)
+        if i < 0:
+            raise KeyError(f"{path}: no tensor {name!r}")
+        info = q4_gguf_tensor_info(h, i)
+        if info["type"] != GGUF_TYPE_Q4_0 or len(info["dims"]) != 2:
+            raise ValueError(f"{name}: not a 2-D Q4_0 tensor (type {info['type']}, dims {info['dims']})")
+        k, n = info["dims"]
+        blocks = np.empty((n, k // 32, 18), dtype=np.uint8)
+        q4_gguf_read_tensor(h, i, blocks, blocks.nbytes)
+        return blocks, n, k
+    finally:
+        q4_gguf_close(h)
+
+
+def load_q4_0_packed(path: str, name: str, stream=None):
+    """(W_packed, n, k): a Q4_0 tensor of a GGUF file, copied to the current
+    device and packed once by q4_0_pack (torch holds the device memory)."""
+    import torch
+    blocks, n, k = gguf_q4_0_blocks(path, name)
+    dev_blocks = torch.from_numpy(blocks.reshape(-1)).cuda()
+    W = torch.empty(q4_0_packed_size(n, k), dtype=torch.uint8, device="cuda")
+    q4_0_pack(W, dev_blocks, n, k, stream)
+    return W, n, k

@@ -420,6 +420,8 @@ Q4MM_API const char *q4_status_string(int status)
     case Q4_ERR_DEVICE_TIMEOUT: return "a device-side wait ran out of time";
     case Q4_ERR_WORKSPACE: return "workspace missing or too small";
     case Q4_ERR_NO_MEMORY: return "out of device memory";
+    case Q4_ERR_IO: return "file could not be opened or read";
+    case Q4_ERR_FORMAT: return "file breaks the GGUF layout";
     default: return "unknown status";
     }
 }

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(q4lib):
 
 
 def test_status_strings(q4lib):
-    for code in range(8):
+    for code in range(10):
         assert q4lib.q4_status_string(code) not in ("", "unknown status")
     assert q4lib.q4_status_string(99) == "unknown status"
 
