@@ -301,7 +301,8 @@ typedef struct q4_gguf q4_gguf;
  * read. Every size is checked against the file: a file that breaks the
  * layout (bad magic, version other than 2 or 3, a string, array or tensor
  * reaching past the end, a descriptor offset not a multiple of
- * general.alignment) gives Q4_ERR_FORMAT; a file that cannot be read,
+ * general.alignment, an array of arrays, more than 4 dimensions) gives
+ * Q4_ERR_FORMAT; a file that cannot be read,
  * Q4_ERR_IO. On success *out owns the parsed file; release it with
  * q4_gguf_close. */
 Q4MM_API int q4_gguf_open(const char *path, q4_gguf **out);

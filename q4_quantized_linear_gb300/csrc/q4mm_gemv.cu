@@ -5,9 +5,10 @@
 // columns cost what one did; goinfer ch. 10, "What the kernels are": the
 // quantised mat-vec is the decode workhorse), so the design goal is to
 // consume a packed record at the rate one SM's share of HBM delivers it with
-// as few instructions as possible. Two modes share the warps, ring and
-// reductions: fp32 FMAs on the CUDA cores (m <= 4, below) and the record-MMA
-// mode on the warp-level tensor core (m <= 16, further down).
+// as few instructions as possible. Three modes share the warps, ring and
+// reductions: fp32 FMAs on the CUDA cores (m <= 4, below), the record-MMA
+// mode on the warp-level tensor core (m <= 16, further down) and its W4A8
+// form (X coded to int8 per block, integer block dots; q4_0_matmul_w4a8).
 //
 // CUDA-core arithmetic. A weight is (q - 8) * d. One lop3 per weight ORs the nibble,
 // left where it lies in its 32-bit word (bit offset s <= 16), into the fp32
