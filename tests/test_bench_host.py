@@ -62,3 +62,16 @@ def test_reference_sample_is_bounded(steps, warmup, t):
     assert 64 <= rows <= 2048 and rows % 64 == 0
     est = (steps + warmup) * t * rows / 2048
     assert est <= 130 or rows == 64
+
+
+def test_kernel_hash_ignores_comments_and_blank_space_only():
+    import bench
+    code = "__global__ void k(float *y) {\n    y[0] = 1.0f;   // one\n}\n"
+    commented = "/* a kernel */\n__global__ void k(float *y)\n{\n  y[0] = 1.0f; // the value one\n}\n"
+    changed = "__global__ void k(float *y) {\n    y[0] = 2.0f;\n}\n"
+    h = bench.source_code_hash([("a.cu", code)])
+    assert bench.source_code_hash([("a.cu", commented)]) == h
+    assert bench.source_code_hash([("a.cu", changed)]) != h
+    assert bench.source_code_hash([("b.cu", code)]) != h
+    # the reader of GGUF files launches nothing: it is left out of the hash
+    assert "q4mm_gguf.cu" in bench.HOST_ONLY_SOURCES
