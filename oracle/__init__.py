@@ -18,6 +18,9 @@ Functions and the passages they follow:
       scale amax / 127), integer dot products, fp64 outer sums (goinfer ch.
       10 "Which kernel runs is a runtime decision"; rembed "Architecture",
       "int8 quantization"; the coding rule is this oracle's reading).
+  matmul_experts -- the expert-grouped product (golem-server, "Several
+      conversations, in one pass"): rows grouped by expert, each group the
+      plain product against its expert's weights.
   pack_reference -- byte-exact reference of the CUDA library's packed layout
       (goinfer ch. 10 "Making Go fast enough": weights repacked for the
       kernel's access order), written from the layout's specification.
@@ -191,4 +194,25 @@ def matmul_w4a8(blocks: np.ndarray, X: np.ndarray, n: int, k: int, nthreads: int
     rc = _load().q4o_matmul_w4a8(_ptr(blocks), _ptr(X), m, k, n, _ptr(Y), _ptr(B), nthreads)
     if rc != 0:
         raise ValueError("bad sizes")
+    return Y, B
+
+
+def matmul_experts(expert_blocks, X: np.ndarray, offsets, n: int, k: int):
+    """Expert-grouped product (golem-server, "Several conversations, in one
+    pass": a mixture reads each expert once for the columns that chose it):
+    X's rows are grouped by expert, rows offsets[e] .. offsets[e+1]-1 going to
+    expert e, and Y[r] = X[r] . W_e^T for those rows. Each group is the plain
+    product above on its rows. Returns (Y, B)."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    offsets = [int(o) for o in offsets]
+    if offsets[0] != 0 or offsets[-1] != X.shape[0] or any(a > b for a, b in zip(offsets, offsets[1:])):
+        raise ValueError("offsets must rise from 0 to the row count")
+    if len(offsets) != len(expert_blocks) + 1:
+        raise ValueError("one offset per expert, plus the end")
+    Y = np.zeros((X.shape[0], n), dtype=np.float64)
+    B = np.zeros((X.shape[0], n), dtype=np.float64)
+    for e, blocks in enumerate(expert_blocks):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            Y[a:b], B[a:b] = matmul(blocks, X[a:b], n, k)
     return Y, B
