@@ -290,10 +290,30 @@ def pin_w4a8_quantization_bound(orc):
     assert np.all(np.abs(Y8 - Y) <= bound * (1 + 1e-9) + 1e-12), "W4A8 within the coding bound"
 
 
+def pin_experts_offsets(orc):
+    """Expert grouping: with every expert holding the same weights the grouped
+    product is the plain one; changing one expert's weights changes exactly
+    its own rows; empty groups are allowed."""
+    n, k = 23, 96
+    X = synth.activations(9, k, seed=91)
+    W = synth.q4_0_blocks(n, k, seed=92)
+    offsets = [0, 2, 2, 7, 9]
+    Y, _ = orc.matmul(W, X, n, k)
+    Ye, _ = orc.matmul_experts([W, W, W, W], X, offsets, n, k)
+    assert np.array_equal(Ye, Y), "same weights: grouped == plain"
+    W2 = synth.q4_0_blocks(n, k, seed=93)
+    Ye2, _ = orc.matmul_experts([W, W, W2, W], X, offsets, n, k)
+    changed = np.any(Ye2 != Ye, axis=1)
+    assert np.array_equal(changed, np.array([r in range(2, 7) for r in range(9)])), "one expert's rows only"
+    Y2, _ = orc.matmul(W2, X, n, k)
+    assert np.array_equal(Ye2[2:7], Y2[2:7]), "those rows are the plain product with that expert"
+
+
 PINS = [pin_golden_block, pin_format_facts, pin_all_eights_is_zero, pin_nibble_order,
         pin_fp16_exhaustive, pin_exact_integer, pin_numpy_special_case, pin_invariants,
         pin_sampled_matches_full, pin_w4a8_golden, pin_w4a8_all_eights_is_zero,
-        pin_w4a8_integer_case_is_the_exact_product, pin_w4a8_homogeneity_and_nan, pin_w4a8_quantization_bound]
+        pin_w4a8_integer_case_is_the_exact_product, pin_w4a8_homogeneity_and_nan, pin_w4a8_quantization_bound,
+        pin_experts_offsets]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
