@@ -112,8 +112,8 @@ def source_code_hash(texts):
     return h.hexdigest()[:16]
 
 
-# host-only sources that launch nothing: excluded from the kernel hash
-HOST_ONLY_SOURCES = {"q4mm_gguf.cu"}
+# host-only sources (no kernels, no plans): excluded from the kernel hash
+HOST_ONLY_SOURCES = {"q4mm_gguf.cu", "q4mm_experts.cu"}
 
 
 def kernel_source_hash():

@@ -150,6 +150,27 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
                             int64_t m, int64_t k, int64_t n,
                             void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
 
+/* Expert-grouped product (a mixture of experts): X's rows are grouped by
+ * expert, rows offsets[e] .. offsets[e+1] - 1 going to expert e, and
+ * Y[r] = X[r] . W_e^T for those rows. golem-server, "Several conversations,
+ * in one pass": a mixture answers a single column by reading the matrices it
+ * was routed to and a prompt by reading each expert once for the columns
+ * that chose it; the two costs cross near thirty-two columns. Here each
+ * expert's weights are read once for its rows, by the decode kernels for up
+ * to 16 rows and the tensor-core GEMM above (one launch sequence per expert
+ * with rows), with q4_0_matmul's precision for each group's size.
+ *   W_packed: host array of n_experts device pointers, each packed by
+ *   q4_0_pack for (n, k), 16-byte aligned (an expert with no rows may be
+ *   NULL).
+ *   offsets: host array of n_experts + 1 row offsets, offsets[0] = 0,
+ *   non-decreasing; the row count is offsets[n_experts].
+ *   X: device fp32 [rows x k], 16-byte aligned; Y: device fp32 [rows x n],
+ *   overwritten, 4-byte aligned.
+ * Every argument is checked before anything is launched. Scratch: as
+ * q4_0_matmul (the library's workspace, for groups of more than 16 rows). */
+Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t n_experts, const int64_t *offsets,
+                                 const float *X, float *Y, int64_t k, int64_t n, q4mm_stream_t stream);
+
 /* W4A8: Y[m x n] = X[m x k] . W^T with X coded to int8 first, so that every
  * block's dot product is an integer one. The pages name the integer dot
  * product (goinfer ch. 10, "Which kernel runs is a runtime decision": the

@@ -39,6 +39,7 @@ _SIGS = {
     "q4_0_matmul": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_ws": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "q4_0_matmul_w4a8": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "q4_0_matmul_experts": (_INT, [ctypes.POINTER(_P), _I64, ctypes.POINTER(_I64), _P, _P, _I64, _I64, _P]),
     "q4_0_matmul_static_scratch": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots_ws": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P, _SZ, _P]),
@@ -143,6 +144,18 @@ def q4_0_unpack(blocks, W_packed, n: int, k: int, stream=None, check: bool = Tru
 def q4_0_matmul(W_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:
     rc = _lib.q4_0_matmul(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _stream(stream))
     return _check(rc, "q4_0_matmul") if check else rc
+
+
+def q4_0_matmul_experts(W_list, offsets, X, Y, k: int, n: int, stream=None, check: bool = True) -> int:
+    """W_list: one packed weight buffer per expert (None for an expert with no
+    rows); offsets: n_experts + 1 row offsets into X and Y."""
+    E = len(W_list)
+    ws = (_P * E)(*[_addr(w) for w in W_list])
+    offs = (_I64 * len(offsets))(*[int(o) for o in offsets])
+    if len(offsets) != E + 1:
+        raise ValueError("one offset per expert, plus the end")
+    rc = _lib.q4_0_matmul_experts(ws, E, offs, _addr(X), _addr(Y), k, n, _stream(stream))
+    return _check(rc, "q4_0_matmul_experts") if check else rc
 
 
 def q4_0_matmul_w4a8(W_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:

@@ -73,6 +73,16 @@ def test_w4a8_rejects_bad_arguments_on_the_host(q4lib, args, code):
     assert q4lib.q4_0_matmul_w4a8(*args, stream=0, check=False) == code
 
 
+@pytest.mark.parametrize("W,offsets,code", [
+    ([0x1000, 0x1000], [1, 2, 3], 1),           # offsets do not start at 0
+    ([0x1000, 0x1000], [0, 3, 2], 1),           # offsets fall
+    ([0x1000, 0], [0, 2, 3], 1),                # an expert with rows has no weights
+    ([0x1000, 0x1008], [0, 2, 3], 2),           # weights not 16-byte aligned
+])
+def test_experts_reject_bad_arguments_on_the_host(q4lib, W, offsets, code):
+    assert q4lib.q4_0_matmul_experts(W, offsets, 0x1000, 0x1000, 64, 64, stream=0, check=False) == code
+
+
 def test_batched_slots_rejects_bad_leading_dimensions(q4lib):
     # ldx < k, ldx % 4 != 0, ldy < n, null slot ids
     assert q4lib.q4_0_matmul_batched_slots(0x1000, 0x1000, 32, 0x1000, 2, 0x1000, 64, 64, 64,

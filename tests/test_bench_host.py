@@ -73,5 +73,6 @@ def test_kernel_hash_ignores_comments_and_blank_space_only():
     assert bench.source_code_hash([("a.cu", commented)]) == h
     assert bench.source_code_hash([("a.cu", changed)]) != h
     assert bench.source_code_hash([("b.cu", code)]) != h
-    # the reader of GGUF files launches nothing: it is left out of the hash
-    assert "q4mm_gguf.cu" in bench.HOST_ONLY_SOURCES
+    # host-only sources (the GGUF reader, the expert loop over q4_0_matmul)
+    # hold no kernels or plans: they are left out of the hash
+    assert {"q4mm_gguf.cu", "q4mm_experts.cu"} <= bench.HOST_ONLY_SOURCES

@@ -309,3 +309,28 @@ def test_bounded_wait_reports_timeout_and_context_survives(q4lib, oracle_mod):
     Y = run_matmul(q4lib, pack_dev(q4lib, blocks, n, k), X, n)
     Yr, B = oracle_mod.matmul(blocks, X, n, k)
     assert_parity(Y, Yr, B, m, "after timeout")
+
+
+# -------------------------------------------------------- expert groups ----
+
+def test_expert_groups_match_the_oracle(q4lib, oracle_mod):
+    """Rows grouped by expert, groups of 0 to 40 rows (decode and prefill
+    sizes, empty experts), each checked at its size's tolerance."""
+    n, k = 200, 1056
+    sizes = [0, 1, 3, 16, 17, 40, 0, 5]
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    rows = int(offsets[-1])
+    experts = [synth.q4_0_blocks(n, k, seed=700 + e) for e in range(len(sizes))]
+    W = [pack_dev(q4lib, b, n, k) if s else None for b, s in zip(experts, sizes)]
+    X = synth.activations(rows, k, seed=701)
+    Xd = to_dev(X)
+    Y = torch.full((rows, n), float("nan"), dtype=torch.float32, device="cuda")
+    q4lib.q4_0_matmul_experts(W, offsets, Xd, Y, k, n)
+    torch.cuda.synchronize()
+    assert q4lib.q4_last_device_status(clear=True) == 0
+    Y = Y.cpu().numpy()
+    Yr, B = oracle_mod.matmul_experts(experts, X, offsets, n, k)
+    for e, s in enumerate(sizes):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if s:
+            assert_parity(Y[a:b], Yr[a:b], B[a:b], s, f"expert {e} ({s} rows)")
