@@ -21,6 +21,9 @@ Functions and the passages they follow:
   matmul_experts -- the expert-grouped product (golem-server, "Several
       conversations, in one pass"): rows grouped by expert, each group the
       plain product against its expert's weights.
+  quantize_w_int8 / matmul_w8 -- per-output-channel symmetric int8 weights
+      and their product with fp32 X (rembed "Architecture", "int8
+      quantization"; the rounding rule is this oracle's reading).
   pack_reference -- byte-exact reference of the CUDA library's packed layout
       (goinfer ch. 10 "Making Go fast enough": weights repacked for the
       kernel's access order), written from the layout's specification.
@@ -216,3 +219,29 @@ def matmul_experts(expert_blocks, X: np.ndarray, offsets, n: int, k: int):
         if b > a:
             Y[a:b], B[a:b] = matmul(blocks, X[a:b], n, k)
     return Y, B
+
+
+def quantize_w_int8(W: np.ndarray):
+    """Per-output-channel symmetric int8 weights (rembed "Architecture",
+    "int8 quantization": dense weights quantised at load to per-output-channel
+    symmetric int8, one per-channel multiply in the epilogue). The pages print
+    no rounding rule; the reading taken, per row j of W [n x k], in fp32:
+    amax = max |w|, scale s = amax / 127, code c = round-half-even(w * (127 /
+    amax)); a row with amax = 0 has codes 0 and scale 0. Returns (codes int8
+    [n x k], scales fp32 [n])."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    amax = np.abs(W).max(axis=1).astype(np.float32)
+    inv = np.zeros_like(amax)
+    nz = amax > 0
+    inv[nz] = np.float32(127.0) / amax[nz]
+    codes = np.rint(W * inv[:, None]).astype(np.int8)
+    scales = (amax / np.float32(127.0)).astype(np.float32)
+    return codes, scales
+
+
+def matmul_w8(codes: np.ndarray, scales: np.ndarray, X: np.ndarray):
+    """Y[t][j] = s_j * sum_c X[t][c] * code[j][c], fp64, with B = sum |terms|."""
+    Xd = np.asarray(X, dtype=np.float64)
+    Cd = np.asarray(codes, dtype=np.float64)
+    s = np.asarray(scales, dtype=np.float64)
+    return (Xd @ Cd.T) * s[None, :], (np.abs(Xd) @ np.abs(Cd).T) * np.abs(s)[None, :]

@@ -309,11 +309,41 @@ def pin_experts_offsets(orc):
     assert np.array_equal(Ye2[2:7], Y2[2:7]), "those rows are the plain product with that expert"
 
 
+def pin_w8_codes_and_product(orc):
+    """Per-channel int8 weights: a row whose largest |w| is 127 keeps integer
+    weights as they are (scale 1), so the product is X . W^T exactly;
+    hand-derived ties (amax 127: 2.5 -> 2, 3.5 -> 4, -0.5 -> 0, -1.5 -> -2)
+    and one scale per row (a row with amax 1 gets scale fp32(1/127) and codes
+    127, 64 for 1, 0.5); a zero row gives zeros; the coding bound holds."""
+    W = np.array([[127.0, 2.5, 3.5, -0.5, -1.5] + [0.0] * 27,
+                  [1.0, 0.5] + [0.0] * 30,
+                  [0.0] * 32], dtype=np.float32)
+    codes, scales = orc.quantize_w_int8(W)
+    assert list(codes[0, :5]) == [127, 2, 4, 0, -2], "round half to even"
+    assert list(codes[1, :2]) == [127, 64] and scales[1] == np.float32(1) / np.float32(127), "per-row scale"
+    assert scales[0] == 1.0 and scales[2] == 0.0 and not codes[2].any(), "scale 1 and the zero row"
+    rng = np.random.default_rng(95)
+    Wi = rng.integers(-126, 127, size=(7, 64)).astype(np.float32)
+    Wi[:, 0] = 127.0
+    Xi = rng.integers(-20, 21, size=(3, 64)).astype(np.float32)
+    c, s = orc.quantize_w_int8(Wi)
+    Y, B = orc.matmul_w8(c, s, Xi)
+    exact = (Xi.astype(np.int64) @ Wi.astype(np.int64).T).astype(np.float64)
+    assert np.array_equal(Y, exact) and np.all(B >= np.abs(Y)), "integer rows are exact"
+    Wf = synth.activations(9, 128, seed=96)
+    X = synth.activations(4, 128, seed=97)
+    c, s = orc.quantize_w_int8(Wf)
+    Y8, _ = orc.matmul_w8(c, s, X)
+    bound = (np.abs(X.astype(np.float64)) @ np.ones((128, 9))) * (s.astype(np.float64) / 2)[None, :]
+    assert np.all(np.abs(Y8 - X.astype(np.float64) @ Wf.astype(np.float64).T) <= bound * (1 + 1e-9) + 1e-12), \
+        "within half a step per weight"
+
+
 PINS = [pin_golden_block, pin_format_facts, pin_all_eights_is_zero, pin_nibble_order,
         pin_fp16_exhaustive, pin_exact_integer, pin_numpy_special_case, pin_invariants,
         pin_sampled_matches_full, pin_w4a8_golden, pin_w4a8_all_eights_is_zero,
         pin_w4a8_integer_case_is_the_exact_product, pin_w4a8_homogeneity_and_nan, pin_w4a8_quantization_bound,
-        pin_experts_offsets]
+        pin_experts_offsets, pin_w8_codes_and_product]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
