@@ -43,6 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Q4_0 weight GB/s (% HBM peak) at m=1..16; prefill TFLOP/s (% bf16 peak)"
 L2_BYTES = 129 * 1024 * 1024
+SLEEP_CYCLES = 200_000          # about 0.1 ms of device time before a timed region
 HEADLINE = dict(name="decode GEMV, FFN up-projection", m=1, n=9728, k=2560)
 WORKLOADS = {
     "decode": HEADLINE,
@@ -77,13 +78,10 @@ def weight_bytes(n, k):
 
 
 def decode_kernel_name(m, n=0, sm_count=152):
-    """The kernel the library's automatic dispatch runs for m token rows of
-    an n-row layer."""
+    """The kernel the library's automatic dispatch runs for m token rows."""
     if m > 16:
         return "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)"
-    if m <= 4 or (m <= 8 and (n + 127) // 128 <= 2 * sm_count):
-        return "gemv_kernel<m, true> (q4mm_gemv.cu, whole records per warp on the warp-level MMA)"
-    return "mmv_kernel (q4mm_mmv.cu, row-tiled warp-level MMA)"
+    return "matvec_kernel (q4mm_matvec.cu, whole records per warp, exact block sums on the warp-level MMA)"
 
 
 def load_peaks():
@@ -290,6 +288,10 @@ def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None, b
         barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
+        # a device-side pause first, so that the graphs are queued before the
+        # start event runs: the timed region holds the steps, not the host's
+        # launch of the first graph
+        torch.cuda._sleep(SLEEP_CYCLES)
         start.record(stream)
         for _ in range(steps // per_graph):
             g_full.replay()
@@ -303,28 +305,74 @@ def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None, b
     return start.elapsed_time(end) / 1e3, clocks
 
 
-def time_e2e(q4lib, wl, steps, stream):
-    """Public API with pinned host buffers: H2D of X, the call, D2H of Y."""
+def time_e2e(q4lib, wl, steps, stream, per_graph=200):
+    """Public API with pinned host buffers: every step copies X host -> device,
+    calls the layer and copies Y device -> host, all inside the timed region
+    (captured as CUDA graphs of up to per_graph steps, like the device-side
+    timing)."""
     import torch
     Xh = torch.from_numpy(wl.X).pin_memory()
     Yh = torch.empty((wl.m, wl.n), dtype=torch.float32).pin_memory()
+
+    def one(i):
+        wl.Xd.copy_(Xh, non_blocking=True)
+        wl.step(q4lib, i, stream.cuda_stream)
+        Yh.copy_(wl.Yd, non_blocking=True)
+
+    per_graph = max(1, min(per_graph, steps))
     with torch.cuda.stream(stream):
         for i in range(3):
-            wl.Xd.copy_(Xh, non_blocking=True)
-            wl.step(q4lib, i, stream.cuda_stream)
-            Yh.copy_(wl.Yd, non_blocking=True)
+            one(i)
+    torch.cuda.synchronize()
+    graphs = {}
+
+    def graph(count):
+        if count not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(count):
+                        one(i)
+            graphs[count] = g
+        return graphs[count]
+
+    g_full = graph(per_graph)
+    rest = steps % per_graph
+    g_rest = graph(rest) if rest else None
+    with torch.cuda.stream(stream):
+        g_full.replay()
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        torch.cuda._sleep(SLEEP_CYCLES)
         start.record(stream)
-        for i in range(steps):
-            wl.Xd.copy_(Xh, non_blocking=True)
-            wl.step(q4lib, i, stream.cuda_stream)
-            Yh.copy_(wl.Yd, non_blocking=True)
+        for _ in range(steps // per_graph):
+            g_full.replay()
+        if g_rest is not None:
+            g_rest.replay()
         end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / 1e3, Xh.numel() * 4, Yh.numel() * 4
+
+
+def time_single(q4lib, wl, stream, trials=50):
+    """Latency of one isolated call: the device idle before and after, CUDA
+    events around the launch on its stream; the median over trials."""
+    import torch
+    out = []
+    for i in range(trials + 3):
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            wl.step(q4lib, i, stream.cuda_stream)
+            end.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            out.append(start.elapsed_time(end) * 1e3)
+    return statistics.median(out)
 
 
 def run_sweep(q4lib, stream, peaks):
@@ -342,6 +390,9 @@ def run_sweep(q4lib, stream, peaks):
         t = sec / steps
         rec = dict(cfg, steps=steps, weight_copies=wl.copies, us_per_call=t * 1e6,
                    weight_gbs=wb / t / 1e9, tokens_per_s=m / t)
+        if n * k <= 1 << 20:
+            # a layer this small is a latency case: one isolated call as well
+            rec["single_call_latency_us"] = time_single(q4lib, wl, stream)
         if m <= 16:
             rec["frac_hbm"] = rec["weight_gbs"] / peaks["hbm_gbs"]
         else:
@@ -353,36 +404,57 @@ def run_sweep(q4lib, stream, peaks):
     return out
 
 
-def cpu_baseline(cfg, gpu_Y=None, tensor=False, seconds=10.0):
-    """Oracle throughput on the host cores (bounded sample), and, when the
-    GPU result is given, its max error over tolerance against the oracle."""
+def cpu_baseline(cfg, gpu_Y=None, tensor=False, run_seconds=1.5):
+    """The oracle (fp64, fixed order) timed on the host cores: single-threaded
+    and on every thread it may use, the median of three runs each, each run a
+    bounded sample (repeated calls on the leading rows of W for about
+    run_seconds). With the GPU result given, also its max error over
+    tolerance against the oracle on the rows the oracle computed."""
     import oracle
     from q4_quantized_linear_gb300 import synth
     m, n, k = cfg["m"], cfg["n"], cfg["k"]
     oracle.build()
     blocks = synth.q4_0_blocks(n, k, seed=0)
     X = synth.activations(m, k, seed=0)
-    # a bounded sample: leading rows of W, enough for about `seconds` of work
-    rows = n if m * n * k <= 2e9 else max(64, int(2e9 / (m * k)) // 64 * 64)
-    reps = 0
-    t0 = time.perf_counter()
-    Yr = B = None
-    while True:
-        Yr, B = oracle.matmul(blocks[:rows], X, rows, k)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or reps >= 1000:
-            break
-    if tensor:
-        value, unit = reps * 2.0 * m * rows * k / el / 1e12, "TFLOP/s"
-    else:
-        value, unit = reps * weight_bytes(rows, k) / el / 1e9, "GB/s"
-    res = {"value": value, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
-           "sample": f"{reps} oracle runs of m={m} x rows 0..{rows - 1} of n={n}, k={k} "
-                     f"({el:.1f} s, fp64, fixed order)"}
+
+    def rate(rows, reps, el):
+        if tensor:
+            return reps * 2.0 * m * rows * k / el / 1e12
+        return reps * weight_bytes(rows, k) / el / 1e9
+
+    def runs(rows, nthreads):
+        vals, last = [], None
+        for _ in range(3):
+            reps, t0 = 0, time.perf_counter()
+            while True:
+                last = oracle.matmul(blocks[:rows], X, rows, k, nthreads=nthreads)
+                reps += 1
+                el = time.perf_counter() - t0
+                if el >= run_seconds:
+                    break
+            vals.append(rate(rows, reps, el))
+        return statistics.median(vals), last
+
+    # the sample: leading rows of W, at most what one run covers in a second
+    # (all threads) or a tenth of that (one thread)
+    rows_all = n if m * n * k <= 2e9 else max(64, int(2e9 / (m * k)) // 64 * 64)
+    rows_one = max(64, min(rows_all, int(2e8 / (m * k)) // 64 * 64))
+    v_all, (Yr, B) = runs(rows_all, 0)
+    v_one, _ = runs(rows_one, 1)
+    unit = "TFLOP/s" if tensor else "GB/s"
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        affinity = None
+    res = {"value": v_all, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"median of 3 runs of about {run_seconds} s each: repeated oracle calls (fp64, fixed order) "
+                     f"on m={m} x rows 0..{rows_all - 1} of n={n}, k={k}, all threads",
+           "single_thread": {"value": v_one, "unit": unit, "cores": 1,
+                             "sample": f"median of 3 runs: rows 0..{rows_one - 1}, one thread"},
+           "nproc": os.cpu_count(), "sched_getaffinity": affinity}
     if gpu_Y is not None:
         rtol, atol = (1e-3, 1e-5) if m <= 16 else (1e-2, 1e-4)
-        ratio = float((np.abs(gpu_Y[:, :rows].astype(np.float64) - Yr) / (rtol * B + atol)).max())
+        ratio = float((np.abs(gpu_Y[:, :rows_all].astype(np.float64) - Yr) / (rtol * B + atol)).max())
         res["parity_max_err_over_tol"] = ratio
     return res
 
@@ -441,10 +513,8 @@ def native(args):
     cpu = None if args.no_cpu else cpu_baseline(cfg, gpu_Y, tensor)
     achieved = per_step_units / per_launch
     traffic = profiled_traffic(f"{args.workload}_m{m}_n{n}_k{k}")
-    if tensor:
-        peak, peak_key = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
-    else:
-        peak, peak_key = peaks["hbm_gbs"], "hbm_gbs"
+    # a kernel of tens of microseconds runs at the burst rate
+    peak, peak_key = (peaks["bf16_tflops"], "bf16_tflops") if tensor else (peaks["hbm_gbs"], "hbm_gbs")
     line = {
         "metric": METRIC,
         "value": value,
@@ -456,7 +526,9 @@ def native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if tensor else "f32",
+        # decode: bf16 operands (X split into two bf16 terms per block,
+        # weights exact), fp32 accumulation; prefill: bf16, fp32 accumulation
+        "dtype": "bf16" if tensor else "bf16x2",
         "data": "synthetic",
         "config": {
             "workload": f"{cfg['name']}: Q4_0 W n={n} x k={k}, m={m}",
@@ -498,10 +570,10 @@ def native(args):
 
 def reference_sample_rows(n, steps, warmup, t_2048, budget_s=120.0):
     """Rows of W per reference step so that warmup + steps oracle calls take
-    about budget_s, given t_2048 seconds for a 2048-row call (64-row units,
-    at least 64, at most 2048 and n)."""
+    about budget_s, given t_2048 seconds for a 2048-row call: the whole layer
+    when it fits (64-row units, at least 64, at most n)."""
     rows = int(2048 * budget_s / max((steps + warmup) * t_2048, 1e-9))
-    return max(min(64, n), min(n, 2048, rows // 64 * 64))
+    return max(min(64, n), min(n, rows // 64 * 64))
 
 
 def reference(args):
@@ -518,12 +590,14 @@ def reference(args):
     wb = weight_bytes(n, k)
     blocks = synth.q4_0_blocks(n, k, seed=0)
     X = synth.activations(m, k, seed=0)
-    # Each step is a bounded sample: the leading rows of W, as many as keep
-    # the whole --warmup + --steps run near two minutes (calibrated on 2048).
-    oracle.matmul(blocks[:2048], X, 2048, k)
+    # Each step covers the leading rows of W, as many as keep the whole
+    # --warmup + --steps run near two minutes (the whole layer when it fits;
+    # calibrated on 2048 rows).
+    cal = min(n, 2048)
+    oracle.matmul(blocks[:cal], X, cal, k)
     t0 = time.perf_counter()
-    oracle.matmul(blocks[:2048], X, 2048, k)
-    t_full = time.perf_counter() - t0
+    oracle.matmul(blocks[:cal], X, cal, k)
+    t_full = (time.perf_counter() - t0) * 2048 / cal
     rows = reference_sample_rows(n, args.steps, args.warmup, t_full)
     sample_bytes = weight_bytes(rows, k)
     for _ in range(args.warmup):

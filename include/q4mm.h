@@ -108,8 +108,8 @@ Q4MM_API int q4_0_unpack(void *blocks, const void *W_packed, int64_t n, int64_t 
                          q4mm_stream_t stream);
 
 /* Bytes of device scratch q4_0_matmul_ws / q4_0_matmul_batched_slots_ws need
- * for these sizes: 0 for m <= 16 (decode needs none), the bf16 X image plus a
- * 256 KB reserved region for m > 16. */
+ * for these sizes: 0 for m <= 16 (decode needs none), the bf16 X image for
+ * m > 16. */
 Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
 
 /* Y[m x n] = X[m x k] . W^T, W given in packed form.
@@ -141,24 +141,23 @@ Q4MM_API int q4_0_matmul(const void *W_packed, const float *X, float *Y,
 /* As q4_0_matmul with caller-owned scratch: `workspace` (device, 256-byte
  * aligned) of at least q4_0_matmul_workspace_size(m, k, n) bytes, which may be
  * NULL when that size is 0. The library never allocates in this form.
- * Zero a new workspace once before its first use (cudaMemset): its first
- * 256 KB hold split-sum counters that every completed call leaves at zero, so
- * one workspace serves calls of any shape in turn. After a call that ended in
- * Q4_ERR_DEVICE_TIMEOUT, zero it again. Calls that can run at the same time
- * need distinct workspaces. */
+ * The workspace holds the bf16 image of X that the prefill path (m > 16)
+ * builds; it needs no initialisation (each call writes what it reads), so
+ * one workspace serves calls of any shape in turn. Calls that can run at the
+ * same time need distinct workspaces. */
 Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
                             int64_t m, int64_t k, int64_t n,
                             void *workspace, size_t workspace_bytes, q4mm_stream_t stream);
 
 /* Expert-grouped product (a mixture of experts): X's rows are grouped by
  * expert, rows offsets[e] .. offsets[e+1] - 1 going to expert e, and
- * Y[r] = X[r] . W_e^T for those rows. golem-server, "Several conversations,
- * in one pass": a mixture answers a single column by reading the matrices it
- * was routed to and a prompt by reading each expert once for the columns
- * that chose it; the two costs cross near thirty-two columns. Here each
- * expert's weights are read once for its rows, by the decode kernels for up
- * to 16 rows and the tensor-core GEMM above (one launch sequence per expert
- * with rows), with q4_0_matmul's precision for each group's size.
+ * Y[r] = X[r] . W_e^T for those rows (golem-server, "Several conversations,
+ * in one pass", on mixture layers: the weights an expert contributes are read
+ * once for the columns routed to it). Each expert's weights are read once for
+ * its rows: the experts with 1..16 rows share one launch of the decode
+ * mat-vec per set of up to 32 of them (a thread-block cluster per 128-row
+ * group of an expert), larger groups run the tensor-core GEMM one expert at a
+ * time; each group has q4_0_matmul's precision for its size.
  *   W_packed: host array of n_experts device pointers, each packed by
  *   q4_0_pack for (n, k), 16-byte aligned (an expert with no rows may be
  *   NULL).
@@ -166,7 +165,9 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
  *   non-decreasing; the row count is offsets[n_experts].
  *   X: device fp32 [rows x k], 16-byte aligned; Y: device fp32 [rows x n],
  *   overwritten, 4-byte aligned.
- * Every argument is checked before anything is launched. Scratch: as
+ * The arguments are checked before anything is launched; if a later group
+ * is refused (its plan, or the library workspace while a stream is being
+ * captured), the groups before it have been written. Scratch: as
  * q4_0_matmul (the library's workspace, for groups of more than 16 rows). */
 Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t n_experts, const int64_t *offsets,
                                  const float *X, float *Y, int64_t k, int64_t n, q4mm_stream_t stream);
@@ -195,6 +196,44 @@ Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t n_experts,
 Q4MM_API int q4_0_matmul_w4a8(const void *W_packed, const float *X, float *Y,
                               int64_t m, int64_t k, int64_t n, q4mm_stream_t stream);
 
+/* Per-output-channel int8 weights (rembed "Architecture", "int8 quantization",
+ * the weight-only form: dense weights quantised once at load to symmetric
+ * int8 with one scale per output channel, dequantised in registers, the
+ * channel's scale applied once in the epilogue).
+ *
+ * Bytes the packed form of an n x k fp32 weight matrix occupies: records of
+ * 128 rows x 64 columns of codes, then one fp32 scale per row (rows padded to
+ * a multiple of 128). 0 for invalid sizes (n < 1, k < 32, k % 32 != 0). */
+Q4MM_API size_t q4_w8_packed_size(int64_t n, int64_t k);
+
+/* Quantise W [n x k] (device fp32, row-major, 16-byte aligned, finite) into
+ * W8_packed (device, q4_w8_packed_size bytes, 16-byte aligned; written).
+ * Row j, every step one IEEE fp32 operation: amax = max |w|, scale
+ * s = amax / 127, code c = round-half-even(w * (127 / amax)) (|c| <= 127); a
+ * row with amax = 0 has codes 0 and s = 0. Enqueued on `stream`. */
+Q4MM_API int q4_w8_quantize(void *W8_packed, const float *W, int64_t n, int64_t k, q4mm_stream_t stream);
+
+/* The codes (device int8 [n x k], row-major, 4-byte aligned) and scales
+ * (device fp32 [n]) held in W8_packed: the inverse of q4_w8_quantize's
+ * layout, for checking it. */
+Q4MM_API int q4_w8_unpack(int8_t *codes, float *scales, const void *W8_packed, int64_t n, int64_t k,
+                          q4mm_stream_t stream);
+
+/* Y[m x n] = X[m x k] . W8^T with W8[j][c] = s_j * code[j][c]: the codes are
+ * exact in fp16 and X is split per 64 columns, scaled by a power of two, into
+ * fp16 hi + lo (22 significant bits relative to those columns' largest |x|);
+ * the tensor cores accumulate in fp32 and s_j scales each output once:
+ * |Y - Y_exact| <= 1e-3 * B + 1e-5, B = sum_c |X[t][c] * s_j * code[j][c]|.
+ * NaN and infinity in X propagate.
+ *   W8_packed: as written by q4_w8_quantize for (n, k); X: device fp32 [m x k]
+ *   row-major, 16-byte aligned; Y: device fp32 [m x n], overwritten, 4-byte
+ *   aligned. m >= 0 (m == 0 does nothing), n >= 1, k >= 32, k % 32 == 0.
+ * Runs the decode mat-vec for up to 16 rows of X at a time (a larger m is
+ * taken in launches of 16 rows, or of 8 or 4 where a long k leaves no room
+ * for 16); needs no scratch and allocates nothing. */
+Q4MM_API int q4_w8_matmul(const void *W8_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,
+                          q4mm_stream_t stream);
+
 /* Size of the library's fixed scratch array used by q4_0_matmul_static_scratch. */
 #define Q4_STATIC_SCRATCH_BYTES (8u << 20)
 
@@ -206,10 +245,10 @@ Q4MM_API int q4_0_matmul_w4a8(const void *W_packed, const float *X, float *Y,
  *   Q4_STATIC_SCRATCH_BYTES are refused with Q4_ERR_WORKSPACE before anything
  *   is launched (m = 540, n = 9728, k = 2560 needs about 3 MiB).
  *   Set-up: the first call on a device, with that device current, looks up
- *   the array's address (cudaGetSymbolAddress, return code checked) and
- *   zeroes its reserved head with a synchronous cudaMemset. Make that first
- *   call before any stream capture; later calls only enqueue work on
- *   `stream`.
+ *   the array's address (cudaGetSymbolAddress, return code checked). Make
+ *   that first call before any stream capture; later calls only enqueue work
+ *   on `stream`. The array needs no zeroing: each call writes the part it
+ *   reads.
  *   Races: every call on a device shares the one array, so calls that can
  *   overlap (other streams, other threads) race; calls in one stream are
  *   ordered.
@@ -280,7 +319,12 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
  *                        split into fp16 hi + lo, tcgen05.mma;
  *   Q4_DECODE_RECORD_MMA each warp takes whole records: exact fp16 (q - 8)
  *                        times X split per block into fp16 hi + lo on the
- *                        warp-level MMA, d applied in fp32 per block (m <= 16).
+ *                        warp-level MMA, d applied in fp32 per block (m <= 16);
+ *   Q4_DECODE_MATVEC     the mat-vec: bf16 128 + q times X split per block
+ *                        into fixed-point bf16 hi + lo on the warp-level MMA,
+ *                        the accumulator starting at the bias correction so
+ *                        that every block dot product is exact; four blocks
+ *                        per accumulator tile at m = 1 (m <= 16).
  * The setting is kept per process and applies to launches made after the
  * call. Other values are refused with Q4_ERR_INVALID_ARG. */
 #define Q4_DECODE_AUTO 0
@@ -288,6 +332,7 @@ Q4MM_API int q4_set_weight_prefetch(int enable);
 #define Q4_DECODE_CUDA_CORE 2
 #define Q4_DECODE_TCGEN05 3
 #define Q4_DECODE_RECORD_MMA 4
+#define Q4_DECODE_MATVEC 5
 Q4MM_API int q4_set_decode_kernel(int kind);
 
 /* Profiling builds only (compiled with -DQ4MM_TRACE): kernels launched after

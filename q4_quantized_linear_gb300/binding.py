@@ -39,6 +39,10 @@ _SIGS = {
     "q4_0_matmul": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_ws": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "q4_0_matmul_w4a8": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
+    "q4_w8_packed_size": (_SZ, [_I64, _I64]),
+    "q4_w8_quantize": (_INT, [_P, _P, _I64, _I64, _P]),
+    "q4_w8_unpack": (_INT, [_P, _P, _P, _I64, _I64, _P]),
+    "q4_w8_matmul": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_experts": (_INT, [ctypes.POINTER(_P), _I64, ctypes.POINTER(_I64), _P, _P, _I64, _I64, _P]),
     "q4_0_matmul_static_scratch": (_INT, [_P, _P, _P, _I64, _I64, _I64, _P]),
     "q4_0_matmul_batched_slots": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P]),
@@ -163,6 +167,25 @@ def q4_0_matmul_w4a8(W_packed, X, Y, m: int, k: int, n: int, stream=None, check:
     return _check(rc, "q4_0_matmul_w4a8") if check else rc
 
 
+def q4_w8_packed_size(n: int, k: int) -> int:
+    return int(_lib.q4_w8_packed_size(n, k))
+
+
+def q4_w8_quantize(W8_packed, W, n: int, k: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_w8_quantize(_addr(W8_packed), _addr(W), n, k, _stream(stream))
+    return _check(rc, "q4_w8_quantize") if check else rc
+
+
+def q4_w8_unpack(codes, scales, W8_packed, n: int, k: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_w8_unpack(_addr(codes), _addr(scales), _addr(W8_packed), n, k, _stream(stream))
+    return _check(rc, "q4_w8_unpack") if check else rc
+
+
+def q4_w8_matmul(W8_packed, X, Y, m: int, k: int, n: int, stream=None, check: bool = True) -> int:
+    rc = _lib.q4_w8_matmul(_addr(W8_packed), _addr(X), _addr(Y), m, k, n, _stream(stream))
+    return _check(rc, "q4_w8_matmul") if check else rc
+
+
 def q4_0_matmul_ws(W_packed, X, Y, m: int, k: int, n: int, workspace, workspace_bytes: int,
                    stream=None, check: bool = True) -> int:
     rc = _lib.q4_0_matmul_ws(_addr(W_packed), _addr(X), _addr(Y), m, k, n, _addr(workspace),
@@ -211,6 +234,7 @@ Q4_DECODE_WARP_MMA = 1
 Q4_DECODE_CUDA_CORE = 2
 Q4_DECODE_TCGEN05 = 3
 Q4_DECODE_RECORD_MMA = 4
+Q4_DECODE_MATVEC = 5
 
 
 def q4_set_decode_kernel(kind: int) -> int:

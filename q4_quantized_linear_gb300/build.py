@@ -21,7 +21,7 @@ TRACE_BUILD = os.path.join(PKG, "_build_trace")
 TRACE_LIB = os.path.join(TRACE_BUILD, "libq4mm.so")
 HEADER = os.path.join(ROOT, "include", "q4mm.h")
 
-SOURCES = ["q4mm_api.cu", "q4mm_pack.cu", "q4mm_decode.cu", "q4mm_gemv.cu", "q4mm_mmv.cu", "q4mm_prefill.cu",
+SOURCES = ["q4mm_api.cu", "q4mm_pack.cu", "q4mm_decode.cu", "q4mm_gemv.cu", "q4mm_mmv.cu", "q4mm_matvec.cu", "q4mm_w8.cu", "q4mm_prefill.cu",
            "q4mm_static.cu", "q4mm_gguf.cu", "q4mm_experts.cu"]
 DEPS = ["q4mm_device.cuh", "q4mm_internal.h"]
 

@@ -98,7 +98,8 @@ bool valid_nk(int64_t n, int64_t k)
 }
 
 // Library-owned scratch for the forms without a workspace argument: one
-// buffer per (device, stream), zeroed when created, grown on demand.
+// buffer per (device, stream), grown on demand. Its contents need no
+// initialisation: every call writes the X image it reads.
 int library_workspace(int dev, cudaStream_t s, size_t need, void **out)
 {
     *out = nullptr;
@@ -128,10 +129,6 @@ int library_workspace(int dev, cudaStream_t s, size_t need, void **out)
         cudaGetLastError();
         w.ptr = nullptr;
         return Q4_ERR_NO_MEMORY;
-    }
-    if (cudaMemsetAsync(w.ptr, 0, bytes, s) != cudaSuccess) {
-        cudaGetLastError();
-        return Q4_ERR_CUDA;
     }
     w.bytes = bytes;
     *out = w.ptr;
@@ -185,9 +182,14 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
         // warp-MMA kernel is faster there); the warp-MMA kernel above m = 8
         // (the record-MMA mode, built up to m = 16, was slower at m = 16 on
         // 14336 x 4096, 2560 x 9728 and 151936 x 2560).
-        if (kind == Q4_DECODE_AUTO) {
-            const bool whole = m <= kGemvMaxM || (m <= 8 && a.groups <= 2 * dev.sm_count);
-            kind = whole ? Q4_DECODE_RECORD_MMA : Q4_DECODE_WARP_MMA;
+        if (kind == Q4_DECODE_AUTO) kind = Q4_DECODE_MATVEC;
+        if (kind == Q4_DECODE_MATVEC) {
+            // the mat-vec stages the CTA's slice of X in shared memory; where
+            // no plan leaves room for it (long K at m > 8), the whole-record
+            // kernel, which reads X where it is used, serves the call
+            MatvecPlan vp;
+            if (plan_matvec(m, k, n, dev.sm_count, &vp)) return map_cuda(launch_matvec(vp, a, s));
+            kind = Q4_DECODE_RECORD_MMA;
         }
         if (kind == Q4_DECODE_CUDA_CORE && m > kGemvMaxM) kind = Q4_DECODE_WARP_MMA;
         if (kind == Q4_DECODE_RECORD_MMA && m > kRecordMmaMaxM) kind = Q4_DECODE_WARP_MMA;
@@ -246,6 +248,35 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
 }
 
 } // namespace
+
+// One launch of the mat-vec over an expert set (each expert at most 16
+// rows). Q4_ERR_INVALID_ARG when no plan fits (the caller then runs the
+// experts one by one).
+int launch_expert_set(const ExpertSet &set, int max_m, const float *X, float *Y, int64_t k, int64_t n,
+                      cudaStream_t s)
+{
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    DecodeArgs a{};
+    a.W = set.W[0];
+    a.X = X;
+    a.rows = nullptr;
+    a.ldx = k;
+    a.Y = Y;
+    a.ldy = n;
+    a.status = dev.status;
+    a.wait_ns = g_wait_ns.load();
+    a.m = max_m;
+    a.n = static_cast<int>(n);
+    a.nb = static_cast<int>(k / 32);
+    a.np = static_cast<int>(ceil_div(k, kPairK));
+    a.groups = static_cast<int>(ceil_div(n, kGroupRows));
+    a.prefetch_w = g_prefetch_w.load();
+    MatvecPlan plan;
+    if (!plan_matvec_experts(max_m, k, n, set.count, dev.sm_count, &plan)) return Q4_ERR_INVALID_ARG;
+    return map_cuda(launch_matvec_experts(plan, a, set, s));
+}
 
 TraceSettings trace_settings()
 {
@@ -382,6 +413,76 @@ Q4MM_API int q4_0_matmul_w4a8(const void *W_packed, const float *X, float *Y, in
     return map_cuda(launch_gemv(gp, a, kGemvModeW4A8, s));
 }
 
+Q4MM_API size_t q4_w8_packed_size(int64_t n, int64_t k)
+{
+    if (!valid_nk(n, k)) return 0;
+    return w8_packed_bytes(n, k);
+}
+
+Q4MM_API int q4_w8_quantize(void *W8_packed, const float *W, int64_t n, int64_t k, q4mm_stream_t stream)
+{
+    if (!W8_packed || !W || !valid_nk(n, k)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W8_packed, 16) || !aligned(W, 16)) return Q4_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    return map_cuda(launch_w8_quantize(static_cast<uint8_t *>(W8_packed), W, n, k, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+Q4MM_API int q4_w8_unpack(int8_t *codes, float *scales, const void *W8_packed, int64_t n, int64_t k,
+                          q4mm_stream_t stream)
+{
+    if (!codes || !scales || !W8_packed || !valid_nk(n, k)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W8_packed, 16) || !aligned(codes, 4) || !aligned(scales, 4)) return Q4_ERR_ALIGNMENT;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    return map_cuda(launch_w8_unpack(codes, scales, static_cast<const uint8_t *>(W8_packed), n, k,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+Q4MM_API int q4_w8_matmul(const void *W8_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,
+                          q4mm_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!W8_packed || !X || !Y || m < 0 || m > (int64_t(1) << 24) || !valid_nk(n, k)) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W8_packed, 16) || !aligned(X, 16) || !aligned(Y, 4)) return Q4_ERR_ALIGNMENT;
+    if (m == 0) return Q4_OK;
+    DeviceInfo dev;
+    const int rc = current_device(&dev);
+    if (rc != Q4_OK) return rc;
+    const int64_t groups = ceil_div(n, kW8GroupRows), np = ceil_div(k, kPairK);
+    const float *row_scale = reinterpret_cast<const float *>(static_cast<const uint8_t *>(W8_packed) +
+                                                             static_cast<size_t>(groups * np) * kW8RecordBytes);
+    // up to 16 rows of X per launch, each one weight pass; where no plan fits
+    // a launch of 16 rows (long k), 8 or 4
+    for (int64_t t0 = 0, mt = 0; t0 < m; t0 += mt) {
+        MatvecPlan vp;
+        mt = std::min<int64_t>(16, m - t0);
+        while (!plan_matvec(mt, k, n, dev.sm_count, &vp, kMatvecInt8) && mt > 4) mt = mt > 8 ? 8 : 4;
+        if (!plan_matvec(mt, k, n, dev.sm_count, &vp, kMatvecInt8)) return Q4_ERR_INVALID_ARG;
+        DecodeArgs a{};
+        a.W = static_cast<const uint8_t *>(W8_packed);
+        a.X = X + t0 * k;
+        a.rows = nullptr;
+        a.ldx = k;
+        a.Y = Y + t0 * n;
+        a.ldy = n;
+        a.status = dev.status;
+        a.wait_ns = g_wait_ns.load();
+        a.m = static_cast<int>(mt);
+        a.n = static_cast<int>(n);
+        a.nb = static_cast<int>(k / 32);
+        a.np = static_cast<int>(np);
+        a.groups = static_cast<int>(groups);
+        a.prefetch_w = g_prefetch_w.load();
+        a.row_scale = row_scale;
+        const int e = map_cuda(launch_matvec(vp, a, s));
+        if (e != Q4_OK) return e;
+    }
+    return Q4_OK;
+}
+
 Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y, int64_t m, int64_t k, int64_t n,
                             void *workspace, size_t workspace_bytes, q4mm_stream_t stream)
 {
@@ -465,7 +566,7 @@ Q4MM_API int q4_set_weight_prefetch(int enable)
 
 Q4MM_API int q4_set_decode_kernel(int kind)
 {
-    if (kind < Q4_DECODE_AUTO || kind > Q4_DECODE_RECORD_MMA) return Q4_ERR_INVALID_ARG;
+    if (kind < Q4_DECODE_AUTO || kind > Q4_DECODE_MATVEC) return Q4_ERR_INVALID_ARG;
     g_decode_kernel.store(kind);
     return Q4_OK;
 }

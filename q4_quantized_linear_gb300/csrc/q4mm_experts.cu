@@ -1,17 +1,20 @@
 // q4mm_experts.cu -- the expert-grouped product (host code: it launches only
 // through q4_0_matmul).
 //
-// golem-server, "Several conversations, in one pass": a mixture answers a
-// single column by reading the matrices that column was routed to, and a
-// prompt by reading each expert once for the columns that chose it; the two
-// costs cross near thirty-two columns. Here X's rows come grouped by expert
-// (offsets[e] .. offsets[e+1] - 1 for expert e) and each expert's weights are
-// read once for its rows: q4_0_matmul runs the decode kernels for up to 16
-// rows and the tensor-core GEMM above, so a handful of rows costs a weight
-// read and a prompt-sized group a tiled product.
+// golem-server, "Several conversations, in one pass" (mixture layers): the
+// cost of a mixture layer is set by which expert matrices are read, once per
+// pass, for the columns routed to them, with the page's measured switch from
+// per-column to per-expert work at about thirty-two columns. Here X's rows
+// come grouped by expert (offsets[e] .. offsets[e+1] - 1 for expert e) and
+// each expert's weights are read once for its rows: the experts with up to
+// 16 rows share one launch of the decode mat-vec (a cluster per group of an
+// expert's rows), larger groups run the tensor-core GEMM.
+#include <algorithm>
 #include <cstdint>
+#include <cuda_runtime.h>
 
 #include "../../include/q4mm.h"
+#include "q4mm_internal.h"
 
 namespace {
 
@@ -22,7 +25,8 @@ bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 extern "C" Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t n_experts, const int64_t *offsets,
                                             const float *X, float *Y, int64_t k, int64_t n, q4mm_stream_t stream)
 {
-    // every argument is checked before anything is launched
+    // the arguments are checked before anything is launched; a group refused
+    // later (its plan or the library workspace) leaves earlier groups written
     if (!W_packed || !offsets || !X || !Y || n_experts < 1 || n_experts > (int64_t(1) << 20) || n < 1 || k < 32 ||
         k % 32 != 0 || n > (int64_t(1) << 31) || k > (int64_t(1) << 31))
         return Q4_ERR_INVALID_ARG;
@@ -35,11 +39,43 @@ extern "C" Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t
         }
     }
     if (!aligned_to(X, 16) || !aligned_to(Y, 4)) return Q4_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Experts with 1..16 rows: one launch of the mat-vec per set of up to 32
+    // of them, every expert's weights read once for its rows. Larger groups:
+    // q4_0_matmul each (the tensor-core GEMM).
+    q4::ExpertSet set;
+    int max_m = 0;
+    auto flush = [&]() -> int {
+        if (set.count == 0) return Q4_OK;
+        int rc = q4::launch_expert_set(set, max_m, X, Y, k, n, s);
+        if (rc == Q4_ERR_INVALID_ARG)   // no plan for this shape: one by one
+            for (int i = 0; i < set.count && (rc == Q4_ERR_INVALID_ARG || rc == Q4_OK); ++i)
+                rc = q4_0_matmul(set.W[i], X + static_cast<int64_t>(set.row0[i]) * k,
+                                 Y + static_cast<int64_t>(set.row0[i]) * n, set.m[i], k, n, stream);
+        set.count = 0;
+        max_m = 0;
+        return rc;
+    };
     for (int64_t e = 0; e < n_experts; ++e) {
         const int64_t r0 = offsets[e], m = offsets[e + 1] - offsets[e];
-        if (m == 0) continue;
+        if (m == 0 || m > 16) continue;
+        set.row0[set.count] = static_cast<int>(r0);
+        set.m[set.count] = static_cast<int>(m);
+        set.W[set.count] = static_cast<const uint8_t *>(W_packed[e]);
+        ++set.count;
+        max_m = std::max(max_m, static_cast<int>(m));
+        if (set.count == q4::kMaxExpertSet) {
+            const int rc = flush();
+            if (rc != Q4_OK) return rc;
+        }
+    }
+    int rc = flush();
+    if (rc != Q4_OK) return rc;
+    for (int64_t e = 0; e < n_experts; ++e) {
+        const int64_t r0 = offsets[e], m = offsets[e + 1] - offsets[e];
+        if (m <= 16) continue;
         // row r0 of X starts on a 16-byte boundary: k is a multiple of 32
-        const int rc = q4_0_matmul(W_packed[e], X + r0 * k, Y + r0 * n, m, k, n, stream);
+        rc = q4_0_matmul(W_packed[e], X + r0 * k, Y + r0 * n, m, k, n, stream);
         if (rc != Q4_OK) return rc;
     }
     return Q4_OK;

@@ -22,11 +22,6 @@ constexpr int kRecQs1Off = 2560;       // 16 bytes per row: qs of block 1
 constexpr size_t kSmemOptIn = 232448 - 256;
 constexpr size_t kSmemPerSM = 233472;  // 228 KB per SM
 
-// Workspaces begin with a reserved, zeroed region (kept for split-sum
-// counters of any kernel that needs them), so calls of any shape can share
-// one buffer.
-constexpr size_t kWsReservedBytes = 256 * 1024;
-
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
@@ -79,6 +74,7 @@ struct DecodeArgs {
     int accumulate;        // add into Y instead of overwriting it
     int xs_bytes;          // shared bytes of the staged X image
     int prefetch_w;        // stream W before waiting on the preceding kernel
+    const float *row_scale;   // int8 weights: the rows' scales (nullptr: Q4_0)
     unsigned long long *trace_buf;
     unsigned trace_cap, trace_cta;
 };
@@ -136,6 +132,60 @@ struct MmvPlan {
 bool plan_mmv(int64_t m, int64_t k, int64_t n, int sm_count, MmvPlan *plan);
 cudaError_t launch_mmv(const MmvPlan &plan, const DecodeArgs &args, cudaStream_t s);
 
+// ---------------------------------------------------------------- matvec --
+
+// A set of experts for one launch of the mat-vec: expert i multiplies rows
+// row0[i] .. row0[i] + m[i] - 1 of X (m[i] <= 16) by its weights W[i] into
+// the same rows of Y. count == 0: a plain call.
+constexpr int kMaxExpertSet = 32;
+struct ExpertSet {
+    int count = 0;
+    int row0[kMaxExpertSet] = {};
+    int m[kMaxExpertSet] = {};
+    const uint8_t *W[kMaxExpertSet] = {};
+};
+
+// Weight formats of the mat-vec.
+constexpr int kMatvecQ4 = 0;     // Q4_0 records
+constexpr int kMatvecInt8 = 1;   // per-output-channel int8 records
+
+struct MatvecPlan {
+    int M = 1;             // kernel instance: tokens 1, 2, 4, 8 or 16
+    int fmt = kMatvecQ4;   // weight format
+    int S = 1;             // K slices = cluster size
+    int clusters = 0;      // persistent clusters: cluster c owns groups c, c + clusters, ...
+    int ctas = 0;          // clusters x S
+    int ring = 8;          // weight-record ring depth (multiple of 8)
+    size_t smem = 0;
+};
+
+bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan, int fmt = kMatvecQ4);
+cudaError_t launch_matvec(const MatvecPlan &plan, const DecodeArgs &args, cudaStream_t s);
+// An expert set: every cluster holds one group of one expert (m = the set's
+// largest row count).
+bool plan_matvec_experts(int64_t m, int64_t k, int64_t n, int experts, int sm_count, MatvecPlan *plan);
+cudaError_t launch_matvec_experts(const MatvecPlan &plan, const DecodeArgs &args, const ExpertSet &set,
+                                  cudaStream_t s);
+// The library's launch of an expert set on the current device (status code).
+int launch_expert_set(const ExpertSet &set, int max_m, const float *X, float *Y, int64_t k, int64_t n,
+                      cudaStream_t s);
+
+// ------------------------------------------------ int8 per-channel weights --
+
+// Records of 128 rows x 64 columns of int8 codes (stored as 128 + c), ordered
+// [group][pair]; then one fp32 scale per row of the padded rows.
+constexpr int kW8GroupRows = 128;
+constexpr int kW8RecordBytes = 8192;
+
+inline size_t w8_packed_bytes(int64_t n, int64_t k)
+{
+    const int64_t groups = ceil_div(n, kW8GroupRows), np = ceil_div(k, kPairK);
+    return static_cast<size_t>(groups * np * kW8RecordBytes + groups * kW8GroupRows * 4);
+}
+
+cudaError_t launch_w8_quantize(uint8_t *packed, const float *W, int64_t n, int64_t k, cudaStream_t s);
+cudaError_t launch_w8_unpack(int8_t *codes, float *scales, const uint8_t *packed, int64_t n, int64_t k, cudaStream_t s);
+
 // --------------------------------------------------------------- prefill --
 
 struct PrefillArgs {
@@ -169,7 +219,7 @@ struct PrefillPlan {
     int rowtiles = 0;
     int bring = 0, wring = 0, astages = 0;
     size_t smem = 0;
-    size_t ws_bytes = 0;    // reserved region + X image bytes
+    size_t ws_bytes = 0;    // X image bytes
     size_t ws_ximg_off = 0;
 };
 

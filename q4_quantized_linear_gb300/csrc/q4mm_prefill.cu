@@ -417,8 +417,8 @@ bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *pl
     if (best.smem > kSmemOptIn) return false;
     // one CTA per SM: each holds all 512 tensor-memory columns
     best.smem = std::max<size_t>(best.smem, kSmemPerSM / 2 + 1024);
-    best.ws_ximg_off = kWsReservedBytes;
-    best.ws_bytes = kWsReservedBytes + static_cast<size_t>(best.ts) * np * best.T * 128;
+    best.ws_ximg_off = 0;
+    best.ws_bytes = static_cast<size_t>(best.ts) * np * best.T * 128;
     *plan = best;
     return true;
 }

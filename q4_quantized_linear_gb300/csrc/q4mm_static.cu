@@ -12,7 +12,6 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = Q4_STATIC_SCRATCH_BYTES;
-static_assert(kStaticScratchBytes > q4::kWsReservedBytes, "scratch must hold the reserved head");
 
 // One array per device the library runs on (a __device__ variable exists
 // once in every device context that loads the module).
@@ -28,12 +27,17 @@ extern "C" Q4MM_API int q4_0_matmul_static_scratch(const void *W_packed, const f
                                                   int64_t m, int64_t k, int64_t n, q4mm_stream_t stream)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return Q4_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return Q4_ERR_CUDA;
+    }
     if (dev < 0 || dev >= kMaxDevices) return Q4_ERR_UNSUPPORTED_DEVICE;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
         return Q4_ERR_CUDA;
+    }
     if (major != 10 || minor != 3) return Q4_ERR_UNSUPPORTED_DEVICE;
     // Refuse, before touching anything, a shape whose scratch exceeds the array.
     if (q4_0_matmul_workspace_size(m, k, n) > kStaticScratchBytes) return Q4_ERR_WORKSPACE;
@@ -41,13 +45,13 @@ extern "C" Q4MM_API int q4_0_matmul_static_scratch(const void *W_packed, const f
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_addr[dev]) {
-            // Set-up, once per device, with that device current (not capturable).
+            // Set-up, once per device, with that device current. The array
+            // needs no zeroing: each call writes the part it then reads.
             void *addr = nullptr;
-            if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) return Q4_ERR_CUDA;
-            // A workspace's reserved head must start at zero; the rest is
-            // written by each call before it is read.
-            if (cudaMemset(addr, 0, q4::kWsReservedBytes) != cudaSuccess) return Q4_ERR_CUDA;
-            if (cudaDeviceSynchronize() != cudaSuccess) return Q4_ERR_CUDA;
+            if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) {
+                cudaGetLastError();
+                return Q4_ERR_CUDA;
+            }
             g_addr[dev] = addr;
         }
         scratch = g_addr[dev];

@@ -103,8 +103,8 @@ def test_pack_rejects_bad_arguments_on_the_host(q4lib):
 
 
 def test_decode_kernel_setting_is_checked(q4lib):
-    # 0..4 accepted (host-only setting), anything else refused; default restored
-    for bad in (-1, 5, 16):
+    # 0..5 accepted (host-only setting), anything else refused; default restored
+    for bad in (-1, 6, 16):
         assert q4lib._lib.q4_set_decode_kernel(bad) == 1
-    for good in (1, 2, 3, 4, 0):
+    for good in (1, 2, 3, 4, 5, 0):
         assert q4lib._lib.q4_set_decode_kernel(good) == 0

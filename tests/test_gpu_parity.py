@@ -46,7 +46,7 @@ def test_pack_matches_oracle_layout_and_unpack_inverts(q4lib, oracle_mod, n, k):
 SHAPES = [(1, 32), (64, 64), (65, 96), (200, 1056), (1000, 2080), (333, 4096), (130, 8192 + 64)]
 
 # The decode kernels (m <= 16) selectable through q4_set_decode_kernel.
-DECODE_KERNELS = {"warp_mma": 1, "cuda_core": 2, "tcgen05": 3, "record_mma": 4}
+DECODE_KERNELS = {"warp_mma": 1, "cuda_core": 2, "tcgen05": 3, "record_mma": 4, "matvec": 5}
 
 
 @pytest.fixture(params=sorted(DECODE_KERNELS))
@@ -85,11 +85,15 @@ def test_decode_parity(q4lib, oracle_mod, decode_kernel, m, n, k):
     ("record_mma", 1, 9728, 2560, 1e-4), ("record_mma", 3, 14336, 4096, 1e-4),
     ("record_mma", 6, 2560, 9728, 1e-4), ("record_mma", 8, 14336, 4096, 1e-4),
     ("record_mma", 13, 9728, 2560, 1e-4), ("record_mma", 16, 1000, 2080, 1e-4),
-    ("warp_mma", 9, 14336, 4096, 1e-4), ("warp_mma", 16, 1000, 2080, 1e-4)])
+    ("warp_mma", 9, 14336, 4096, 1e-4), ("warp_mma", 16, 1000, 2080, 1e-4),
+    ("matvec", 1, 9728, 2560, 1e-4), ("matvec", 2, 2560, 9728, 1e-4), ("matvec", 3, 14336, 4096, 1e-4),
+    ("matvec", 6, 2560, 9728, 1e-4), ("matvec", 8, 14336, 4096, 1e-4), ("matvec", 13, 9728, 2560, 1e-4),
+    ("matvec", 16, 1000, 2080, 1e-4)])
 def test_decode_kernel_accuracy_margin(q4lib, oracle_mod, kind, m, n, k, rtol):
     """The CUDA-core kernel forms (q - 8) exactly and multiplies fp32 X
-    unrounded; the warp-MMA kernel forms (q - 8) exactly and keeps 22 bits of
-    X per block: both stay far inside the decode bound (checked at rtol)."""
+    unrounded; the warp-MMA kernels form (q - 8) exactly and keep 22 bits of
+    X per block (16 in the mat-vec's fixed-point split, with exact block dot
+    products): all stay far inside the decode bound (checked at rtol)."""
     blocks = synth.q4_0_blocks(n, k, seed=91)
     X = synth.activations(m, k, seed=92)
     W = pack_dev(q4lib, blocks, n, k)
@@ -334,3 +338,30 @@ def test_expert_groups_match_the_oracle(q4lib, oracle_mod):
         a, b = int(offsets[e]), int(offsets[e + 1])
         if s:
             assert_parity(Y[a:b], Yr[a:b], B[a:b], s, f"expert {e} ({s} rows)")
+
+
+@pytest.mark.parametrize("n,k,sizes", [
+    (130, 640, [1, 0, 2, 3, 4, 5, 8, 16, 1, 9]),                           # one launch for all
+    (200, 1056, [(e * 7) % 17 for e in range(40)]),                         # two sets of <= 32
+    (9728, 2560, [1, 3, 0, 16, 5, 2, 8, 4]),                                # the layer's size
+    (96, 2080, [20, 1, 33, 2]),                                             # with GEMM-sized groups
+])
+def test_expert_sets_match_the_oracle(q4lib, oracle_mod, n, k, sizes):
+    """Experts of up to 16 rows share one launch of the mat-vec per set of
+    up to 32 (a cluster per group of an expert's rows); each group is checked
+    at its size's tolerance, and rows of other groups are not touched."""
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    rows = int(offsets[-1])
+    experts = [synth.q4_0_blocks(n, k, seed=900 + e) if s_ else None for e, s_ in enumerate(sizes)]
+    W = [pack_dev(q4lib, b, n, k) if b is not None else None for b in experts]
+    X = synth.activations(rows, k, seed=901)
+    Y = torch.full((rows, n), float("nan"), dtype=torch.float32, device="cuda")
+    q4lib.q4_0_matmul_experts(W, offsets, to_dev(X), Y, k, n)
+    torch.cuda.synchronize()
+    assert q4lib.q4_last_device_status(clear=True) == 0
+    Y = Y.cpu().numpy()
+    for e, s_ in enumerate(sizes):
+        if s_:
+            a, b = int(offsets[e]), int(offsets[e + 1])
+            Yr, B = oracle_mod.matmul(experts[e], X[a:b], n, k)
+            assert_parity(Y[a:b], Yr, B, s_, f"expert {e} ({s_} rows)")

@@ -1,6 +1,8 @@
 """q4_0_matmul_static_scratch, the form of q4_0_matmul that allocates nothing
-(its scratch is a fixed device array of the library), checked through the C
-ABI against the existing entry point q4_0_matmul on two calls in a row, and
+(its scratch is a fixed device array of the library), for callers that may
+not allocate device memory. Checked through the C ABI on two calls in a row:
+against the CPU oracle at the decode or prefill tolerance, and against the
+existing entry point q4_0_matmul (the same kernels, so the same bits); and
 its refusal of shapes whose scratch does not fit. Collected last, it must
 pass on its own and after every other test."""
 import numpy as np
@@ -36,12 +38,14 @@ def test_static_scratch_matches_matmul_on_two_calls(q4lib, oracle_mod, m, n, k):
         ys = Ys.cpu().numpy().astype(np.float64)
         yr = Yr.cpu().numpy().astype(np.float64)
         assert np.isfinite(ys).all() and np.isfinite(yr).all(), f"call {call}: unwritten outputs"
-        # the tolerance of the existing entry point, with B from the oracle
+        # the same kernels as the existing entry point: the same bits
+        assert np.array_equal(ys.view(np.uint64), yr.view(np.uint64)), f"call {call}: differs from q4_0_matmul"
+        # and the oracle's Y, element by element on a sample, at the tolerance of m
         cnt = 4000
         t = np.concatenate([rng.integers(0, m, cnt), [0, m - 1]])
         j = np.concatenate([rng.integers(0, n, cnt), [0, n - 1]])
-        _, B = oracle_mod.matmul_sampled(blocks, X, n, k, t, j)
-        err = np.abs(ys[t, j] - yr[t, j])
+        Yo, B = oracle_mod.matmul_sampled(blocks, X, n, k, t, j)
+        err = np.abs(ys[t, j] - Yo)
         assert np.all(err <= rtol * B + atol), f"call {call}: max err/tol {float((err / (rtol * B + atol)).max())}"
 
 
