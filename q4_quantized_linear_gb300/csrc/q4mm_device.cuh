@@ -1,7 +1,7 @@
 // q4mm_device.cuh -- inline-PTX helpers for the sm_103a kernels of libq4mm:
 // mbarriers with time-bounded waits, 1-D bulk async copies (TMA engine),
-// proxy fences, programmatic dependent launch, bf16 packing, the legacy
-// warp-level bf16 MMA, and the tcgen05 (5th-gen tensor core / TMEM) calls.
+// proxy fences, programmatic dependent launch, bf16 packing, nibble
+// unpacking, and the tcgen05 (5th-gen tensor core / TMEM) calls.
 #pragma once
 
 #include <cstdint>
@@ -245,13 +245,6 @@ __device__ __forceinline__ uint4 lds128(const void *p)
     return v;
 }
 
-__device__ __forceinline__ uint2 lds64(const void *p)
-{
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
-    return v;
-}
-
 __device__ __forceinline__ void sts128(void *p, uint4 v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -288,13 +281,6 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
-__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t r;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-    return r;
-}
-
 // (w & 0x000F000F) | 0x43004300 : two nibbles into bf16 128 + q (exact).
 __device__ __forceinline__ uint32_t nib2_bf16_biased(uint32_t w)
 {
@@ -355,20 +341,6 @@ __device__ __forceinline__ void unpack_word_f16(uint32_t w, uint32_t v[4])
     v[1] = hfma2_bits(lop3_and_or(w, 0x00F000F0u, magic), k1_16, km72);
     v[2] = hsub2_bits(lop3_and_or(w8, 0x000F000Fu, magic), k1032);
     v[3] = hfma2_bits(lop3_and_or(w8, 0x00F000F0u, magic), k1_16, km72);
-}
-
-// --------------------------------------------------- warp-level bf16 MMA --
-
-// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
-                                               const float c[4])
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
 }
 
 // ------------------------------------------------------------ tcgen05 --

@@ -8,34 +8,39 @@
 // short, because in a stream of calls that work is what one call adds to the
 // next.
 //
-// Arithmetic, exact up to the final scaling. X is the B operand of the warp-
-// level MMA (mma.sync m16n8k16, bf16 x bf16 -> fp32). Each 32-element block of
-// a token row is scaled by a power of two 2^-e (its largest |x| lands in
-// [1, 2)) and split into two fixed-point terms: hi, a multiple of 2^-7, and
-// lo, a multiple of 2^-15 (x - hi rounded to that grid): 16 bits relative to
-// the block's largest |x|. Both are exact in bf16. The A operand is a nibble
-// OR'ed into the bf16 pattern of 128: exactly 128 + q, one lop3 for two
-// weights and no subtraction. The accumulator of a column starts at
-// -136 * (sum of that column's terms over the block), so it ends at
-// sum (q - 8) * term. Every partial sum on the way is a multiple of 2^-7 (hi)
-// or 2^-15 (lo) below 2^15 (2^5), at most 22 significant bits, so fp32 holds
-// each one exactly and the tensor core's summation order cannot change the
-// block's two dot products. They are then added and scaled by d * 2^e in fp32
-// (one rounding each) into the row's fp32 total. All-eights weights give 0
-// exactly, and integer inputs stay integer-exact.
+// Arithmetic (m <= 4), exact up to the final scaling. X is the B operand of
+// the warp-level MMA (mma.sync m16n8k16, fp16 x fp16 -> fp32). Each 32-element
+// block of a token row is scaled by a power of two 2^-e (its largest |x|
+// lands in [1, 2)) and split into two fixed-point terms: hi, a multiple of
+// 2^-7, and lo, a multiple of 2^-15 (x - hi rounded to that grid, kept 2^8
+// larger): 16 bits relative to the block's largest |x|. The A operand is a
+// nibble OR'ed into the fp16 pattern of 1024: exactly 1024 + q for the low
+// nibbles (k-step 0) and, left in place, 1024 + 16q for the high ones
+// (k-step 1, whose X terms are divided by 16): one lop3 for two weights and
+// no subtraction. The accumulator of a column starts at the correction
+// -1032 (sum of its k-step-0 terms) - 1152 (sum of its k-step-1 terms), so it
+// ends at sum (q - 8) * term. Every partial sum on the way is a multiple of
+// 2^-7 below 2^16, so fp32 holds each one exactly and the tensor core's
+// summation order cannot change the block's dot products. They are then added
+// and scaled by d * 2^e in fp32 (one rounding each) into the row's fp32 total.
+// All-eights weights give 0 exactly, and integer inputs stay integer-exact.
 // A block of X that holds a NaN or an infinity switches the CTA to exact
-// weights (bf16 q - 8, one subtraction more per two weights) with a zero
-// starting accumulator, so that infinities meet (q - 8) and d as IEEE
-// arithmetic says; the finite blocks' results are the same bits either way.
+// weights (q - 8, one subtraction more per two weights) with a zero starting
+// accumulator, so that infinities meet (q - 8) and d as IEEE arithmetic says;
+// the finite blocks' results are the same bits either way.
+//
+// Arithmetic (m >= 8), where the MMA count per weight grows with the tokens:
+// one fp16 term per element, x 2^-e with the block's 2^e taken over all the
+// CTA's tokens (relative error at most 2^-11, half the decode bound of 1e-3
+// of sum |x w|), against exact weights q - 8 and 16 (q - 8) with a zero
+// start; the products are exact and the block's sums are fp32 sums.
 //
 // MMA columns. For m <= 4 the hi and lo terms of a (token, block) are two
 // columns of the 8, and the 8 columns hold up to four (token, block) pairs:
 // m = 1 puts a record's two blocks side by side in one accumulator tile
 // (thread t of a quad holds block t), m = 2 the two blocks of two tokens, m = 4
 // one block of four tokens. The weights of a 16 x 16 tile are dequantised once
-// for all of them. For m = 5..16 the columns are tokens and the hi and lo
-// terms are two MMAs into the same accumulator (exact weights, zero start:
-// the partial sums, below 2^9 on a 2^-15 grid, stay exact too).
+// for all of them. For m = 5..16 the columns are tokens, eight per tile.
 //
 // K permutation. Thread (g, t) of a warp (lane 4g + t) holds A rows g and
 // g + 8. Its A registers come straight from word t of the rows' 16 nibble
@@ -51,14 +56,17 @@
 // next's). After the dependency wait the warps stage the CTA's slice of X
 // once as B fragments in shared memory. Warp c owns the records
 // u = c (mod 8) of the CTA's sequence (its groups x its pairs, in that
-// order) and the ring slots they pass through: lane 0 refills a slot with a
-// 1-D bulk copy of the record R places ahead as soon as the warp has read it,
-// so every barrier has one waiter and no copy is in flight when the CTA
+// order) and the ring slots they pass through: lane 0 refills a slot with
+// 1-D bulk copies of the record R places ahead as soon as the warp has read
+// it, so every barrier has one waiter and no copy is in flight when the CTA
 // exits; with weights declared read-only the first R records stream before
 // the dependency wait. A warp takes a record's eight row tiles at once, which
 // gives the scheduler eight independent streams of loads, dequantisation and
-// MMAs. At the end of a group each warp leaves its partial rows in shared
-// memory; one group later warp c sums rows 16c .. 16c + 15 of the eight
+// MMAs. For m >= 8 the items are half records instead (rows 0-63 for warps
+// 0-3, rows 64-127 for warps 4-7, each half its own sequence dealt to its
+// four warps), which halves the registers and shared memory a warp's partial
+// rows take. At the end of a group each warp leaves its partial rows in
+// shared memory; one group later warp c sums rows 16c .. 16c + 15 of the
 // partials in order, then the cluster's slices of them, and writes Y. Every
 // wait is bounded and warp-uniform.
 #include <algorithm>
@@ -67,6 +75,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 
 #include "q4mm_device.cuh"
 #include "q4mm_internal.h"
@@ -81,9 +90,14 @@ constexpr int kSliceRows = kGroupRows / kWarps;  // rows of a group each warp fi
 constexpr int kMaxSlices = 8;
 constexpr int kMaxRing = 32;                     // records; a multiple of kWarps when slots are refilled
 
-// B entries per (record, block): one for m <= 4 (hi and lo are columns), a hi
-// and a lo entry per eight tokens otherwise.
-__host__ __device__ constexpr int entries_per_block(int M) { return M <= 4 ? 1 : 2 * (M / 8); }
+// m >= 8 streams half records: a warp takes rows 0-63 or 64-127 of its
+// records (warps 0-3 and 4-7), so that its partial rows cover 64 rows.
+__host__ __device__ constexpr int halves(int M) { return M >= 8 ? 2 : 1; }
+__host__ __device__ constexpr int item_tiles(int M) { return 8 / halves(M); }   // 16-row tiles of an item
+__host__ __device__ constexpr int item_rows(int M) { return kGroupRows / halves(M); }
+// B entries per (record, block): one for m <= 4 (hi and lo are columns), one
+// per eight tokens otherwise (a single fp16 term).
+__host__ __device__ constexpr int entries_per_block(int M) { return M <= 4 ? 1 : M / 8; }
 // Lanes of an entry that hold X: for m <= 2 only the lanes of the block's own
 // columns (8 for m = 1, 16 for m = 2; the others read zeros and are not
 // stored), all 32 otherwise.
@@ -96,6 +110,12 @@ __host__ __device__ constexpr int entry_bytes(int M) { return entry_lanes(M) * 1
 constexpr int kFmtQ4 = 0;
 constexpr int kFmtW8 = 1;
 __host__ __device__ constexpr int rec_bytes(int F) { return F == kFmtW8 ? kW8RecordBytes : kRecordBytes; }
+// A ring slot holds one item: a record, or half of one (Q4_0: the half's
+// scales, block-0 and block-1 nibbles at 0, 256 and 1280; int8: its 64 rows).
+__host__ __device__ constexpr int slot_bytes(int M, int F) { return rec_bytes(F) / halves(M); }
+constexpr int kHalfQs0Off = 256;
+constexpr int kHalfQs1Off = 1280;
+__host__ __device__ constexpr int max_ring(int M) { return kMaxRing * halves(M); }
 // int8 records: B entries per record (hi and lo columns for m <= 4; a hi and a
 // lo entry per eight tokens otherwise), each 32 lanes x 32 bytes (four k-steps)
 __host__ __device__ constexpr int w8_entries(int M) { return M <= 4 ? 1 : 2 * (M / 8); }
@@ -104,7 +124,7 @@ __host__ __device__ constexpr int xfrag_bytes(int M, int F)
 {
     return F == kFmtW8 ? w8_entries(M) * 1024 : 2 * entries_per_block(M) * entry_bytes(M);
 }
-__host__ __device__ constexpr int xparam_bytes(int M, int F) { return F == kFmtW8 ? M * 4 : 2 * M * (M <= 4 ? 32 : 4); }
+__host__ __device__ constexpr int xparam_bytes(int M, int F) { return F == kFmtW8 ? M * 4 : M <= 4 ? 2 * M * 16 : 8; }
 // The parameter region of a slice, rounded up so that what follows it (row
 // buffers, barriers) stays 16-byte aligned.
 __host__ __device__ constexpr int xparam_region(int M, int F, int Pmax) { return (Pmax * xparam_bytes(M, F) + 15) / 16 * 16; }
@@ -112,13 +132,15 @@ __host__ __device__ constexpr int xparam_region(int M, int F, int Pmax) { return
 __host__ __device__ constexpr int acc_width(int M) { return M <= 4 ? 1 : M / 4; }
 
 struct VSmem {
-    uint8_t *ring;        // [R] records
+    uint8_t *ring;        // [R] slots of slot_bytes (R / halves per half of the warps)
+    int rh;               // slots per half of the warps
     uint4 *bimg;          // [Pmax] x xfrag_bytes: B fragments of X (Q4_0: [2][NQ][entry_lanes];
                           // int8: [entries][32 lanes][2])
-    float4 *xp;           // Q4_0, M <= 4: [Pmax][2][M][2] {the four columns' corrections}, {2^e, 0, 0, 0}
-    float *xs;            // Q4_0, M >= 8: [Pmax][2][M] 2^e; int8: [Pmax][M] 2^e
-    float *part;          // [NB][8][M][128] the warps' partial rows of a group (single-group
-                          // grids with the whole slice in the ring: warp c's first ring slot)
+    float4 *xp;           // Q4_0, M <= 4: [Pmax][2][M] {hi and lo columns' corrections, 2^e, 0}
+    float *xs;            // Q4_0, M >= 8: [Pmax][2] 2^e of a block; int8: [Pmax][M] 2^e
+    float *part;          // [NB][8][M][item_rows] the warps' partial rows of a group
+    bool part_in_ring;    // single-group grids with the whole slice in the ring: warp c's
+                          // partial rows sit in its first ring slot instead
     int part_stride;      // floats from one warp's partial rows to the next's
     float *red;           // [NR][S - 1][M][128] other slices' rows of a group (first CTA)
     int *flag;            // a staged block of X was not finite
@@ -127,6 +149,19 @@ struct VSmem {
     uint64_t *red_full, *red_free;    // [2][8] a row slice's other slices landed / slot free
     uint64_t *red_tx;                 // single-group grids: the other slices' rows landed
 };
+
+// f(integral_constant<int, i>) for i = 0 .. N - 1, each a compile-time index
+// (shared-memory offsets that depend on it fold into the loads).
+template <typename Fn, int... I>
+__device__ __forceinline__ void static_for_impl(Fn &&f, std::integer_sequence<int, I...>)
+{
+    (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, typename Fn>
+__device__ __forceinline__ void static_for(Fn &&f)
+{
+    static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
 
 __device__ __forceinline__ void fail(const DecodeArgs &a) { record_status(a.status, kErrTimeout); }
 
@@ -139,12 +174,6 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity
     return __all_sync(0xFFFFFFFFu, mbar_wait_cluster(bar, parity, limit_ns)) != 0;
 }
 
-__device__ __forceinline__ uint32_t ld32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
 __device__ __forceinline__ uint4 ld128(uint32_t addr)
 {
     uint4 v;
@@ -157,6 +186,23 @@ __device__ __forceinline__ float4 ld128f(uint32_t addr)
     asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
     return v;
 }
+// The same at a compile-time byte offset from `addr` (folded into the load).
+template <int OFF>
+__device__ __forceinline__ uint32_t ld32o(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 ld128o(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr), "n"(OFF));
+    return v;
+}
 __device__ __forceinline__ float2 ld64f(uint32_t addr)
 {
     float2 v;
@@ -164,25 +210,35 @@ __device__ __forceinline__ float2 ld64f(uint32_t addr)
     return v;
 }
 
-// D += A * B, m16n8k16, bf16 operands, fp32 accumulate in place. Volatile, so
-// that a record's MMAs, which consume its shared-memory loads, are issued
-// before the record's slot is refilled.
-__device__ __forceinline__ void mma_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulate in place (exact fp16
-// weights times X's fp16 terms).
+// weights times X's fp16 terms). Volatile, so that an item's MMAs, which
+// consume its shared-memory loads, are issued before its slot is refilled.
 __device__ __forceinline__ void mma_acc_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
     asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
                  "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A * B, m16n8k16, fp16 operands, fp32 result from a zero start.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// (y0, y1) += (v0, v1) * s as one packed fp32 operation (each lane one
+// rounding, as two fmaf).
+__device__ __forceinline__ void fma2(float &y0, float &y1, float v0, float v1, float s)
+{
+    asm("{\n\t.reg .b64 y, v, s;\n\t"
+        "mov.b64 y, {%0, %1};\n\tmov.b64 v, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
+        "fma.rn.f32x2 y, v, s, y;\n\tmov.b64 {%0, %1}, y;\n\t}"
+        : "+f"(y0), "+f"(y1)
+        : "f"(v0), "f"(v1), "f"(s));
 }
 
 // Asynchronous store of one fp32 value into another CTA's shared memory
@@ -216,32 +272,19 @@ __device__ __forceinline__ uint32_t pack_half2_rn(float a, float b)
 }
 
 // Fp16 scale of a row's block from the record's scale word (block 0 in the
-// low half, block 1 in the high half).
+// low half, block 1 in the high half), at a bit offset sh of 0 or 16.
+__device__ __forceinline__ float half_at(uint32_t w, int sh)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> sh)));
+}
+// The same for a block given as 0 or 1.
 __device__ __forceinline__ float half_of(uint32_t w, int hi)
 {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(hi ? (w >> 16) : (w & 0xFFFFu))));
 }
 
 // The eight weights of one word of split-half nibbles (bytes 4t .. 4t+3 of a
-// block's qs) as bf16 pairs in the K permutation: v[0] = (e, e+2),
-// v[1] = (e+16, e+18), v[2] = (e+1, e+3), v[3] = (e+17, e+19), e = 4t.
-// Biased: 128 + q. Exact: q - 8.
-template <bool EXACT>
-__device__ __forceinline__ void weights_of(uint32_t w, uint32_t v[4])
-{
-    v[0] = nib2_bf16_biased(w);
-    v[1] = nib2_bf16_biased(w >> 4);
-    v[2] = nib2_bf16_biased(w >> 8);
-    v[3] = nib2_bf16_biased(w >> 12);
-    if (EXACT) {
-        const uint32_t k136 = 0x43084308u;   // bf16 (136, 136)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = bf16x2_sub(v[i], k136);
-    }
-}
-
-// m <= 4: the eight weights of one word of split-half nibbles (bytes
-// 4t .. 4t+3 of a block's qs) as fp16 pairs, the low nibbles for k-step 0
+// block's qs) as fp16 pairs, the low nibbles for k-step 0
 // and the high ones, in place at bits 4-7, for k-step 1:
 //   k0a = (e, e+2), k0b = (e+1, e+3): 1024 + q;
 //   k1a = (e+16, e+18), k1b = (e+17, e+19): 1024 + 16q;   e = 4t.
@@ -262,19 +305,16 @@ __device__ __forceinline__ void weights_f16(uint32_t w, uint32_t &k0a, uint32_t 
     }
 }
 
-// Stage the CTA's slice of X (pairs p0 .. p0 + P - 1) as B fragments. A task
-// is one (pair, block, token): four lanes of a warp (t = 0..3) hold its 32
-// values, eight each (elements 4t .. 4t+3 and 16 + 4t .. 19 + 4t), agree on
-// its scale by two shuffles, split them into hi and lo and store them where
-// the consumer lanes read them:
-//   m <= 4: entry (p, b), column pair c (c = b for m = 1, 2b + token for
-//           m = 2, token for m = 4): hi at lane 4 (2c) + t, lo at
-//           lane 4 (2c + 1) + t (for m <= 2 the entry stores only the
-//           block's own lanes);
-//   m >= 8: entries (p, b, 2h) (hi) and (p, b, 2h + 1) (lo) of tokens
-//           8h .. 8h + 7: lane 4 (token - 8h) + t.
-// A fragment register holds, for k-step 0, elements (4t, 4t+2) and
-// (16+4t, 18+4t); for k-step 1, (4t+1, 4t+3) and (17+4t, 19+4t).
+// m <= 4: stage the CTA's slice of X (pairs p0 .. p0 + P - 1) as B
+// fragments. A task is one (pair, block, token): four lanes of a warp
+// (t = 0..3) hold its 32 values, eight each (elements 4t .. 4t+3 and
+// 16 + 4t .. 19 + 4t), agree on its scale by two shuffles, split them into hi
+// and lo and store them where the consumer lanes read them: entry (p, b),
+// column pair c (c = b for m = 1, 2b + token for m = 2, token for m = 4): hi
+// at lane 4 (2c) + t, lo at lane 4 (2c + 1) + t (for m <= 2 the entry stores
+// only the block's own lanes). A fragment register holds, for k-step 0,
+// elements (4t, 4t+2) and (4t+1, 4t+3); for k-step 1, the same elements plus
+// 16, divided by 16.
 template <int M>
 __device__ __forceinline__ void stage_x(const DecodeArgs &a, const VSmem &sm, int p0, int P, int w, int lane)
 {
@@ -302,7 +342,7 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const VSmem &sm, in
         for (int i = 0; i < kBatch; ++i) {
             if (e0 + 8 * kWarps * i >= E) break;    // warp-uniform: none of the warp's tasks is left
             const int e = e0 + 8 * kWarps * i + q;
-            const int tok = e % M, pb = e / M, b = pb & 1;
+            const int tok = e % M, pb = e / M;
             unsigned mb = max(absmax_bits(xa[i]), absmax_bits(xb[i]));
             mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
             mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
@@ -313,10 +353,10 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const VSmem &sm, in
             const float sd = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);   // 2^-ex
             const float v[8] = {xa[i].x, xa[i].y, xa[i].z, xa[i].w, xb[i].x, xb[i].y, xb[i].z, xb[i].w};
             float hi[8], lo[8];
-            // m <= 4 keeps lo scaled by 2^8 (on the same 2^-7 grid as hi); the
+            // lo is kept scaled by 2^8 (on the same 2^-7 grid as hi); the
             // high-nibble half of the block (elements 16..31, k-step 1) is
             // divided by 16 to meet weights of 1024 + 16q
-            constexpr float kLoScale = M <= 4 ? 256.0f : 1.0f;
+            constexpr float kLoScale = 256.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (fin) {
@@ -329,11 +369,11 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const VSmem &sm, in
                     hi[j] = v[j];
                     lo[j] = 0.f;
                 }
-                if (M <= 4 && j >= 4) hi[j] *= 0.0625f, lo[j] *= 0.0625f;
+                if (j >= 4) hi[j] *= 0.0625f, lo[j] *= 0.0625f;
             }
             uint4 *ent = sm.bimg + static_cast<size_t>(pb * kNQ) * entry_lanes(M);
             const float su = __uint_as_float(static_cast<unsigned>(127 + ex) << 23);   // 2^ex
-            if constexpr (M <= 4) {
+            {
                 // the four columns' sums (k-step 0 and 1, hi and lo), exact:
                 // multiples of 2^-7 or 2^-11 far below 2^24 of them
                 float s0h = hi[0] + hi[1] + hi[2] + hi[3], s0l = lo[0] + lo[1] + lo[2] + lo[3];
@@ -363,33 +403,94 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const VSmem &sm, in
                 ent[4 * (2 * c + 1) + t] = fl;
                 if (t == 0) {
                     // a weight of 1024 + q (k-step 0) or 1024 + 16q against x / 16
-                    // (k-step 1) carries 1032 x or 72 x = 1152 (x / 16) beyond (q - 8) x
-                    float4 *pp = sm.xp + (pb * M + tok) * 2;
-                    pp[0] = fin ? make_float4(-1032.0f * s0h, -1032.0f * s0l, -1152.0f * s1h, -1152.0f * s1l)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                    pp[1] = make_float4(su, 0.f, 0.f, 0.f);
+                    // (k-step 1) carries 1032 x or 72 x = 1152 (x / 16) beyond
+                    // (q - 8) x; each column's correction, a multiple of 2^-4
+                    // below 2^16, is exact
+                    sm.xp[pb * M + tok] = fin ? make_float4(-1032.0f * s0h - 1152.0f * s1h,
+                                                            -1032.0f * s0l - 1152.0f * s1l, su, 0.f)
+                                              : make_float4(0.f, 0.f, su, 0.f);
                 }
-            } else {
-                if (e >= E) continue;
-                uint4 fh, fl;
-                fh.x = pack_bf16x2_rn(hi[0], hi[2]);
-                fh.y = pack_bf16x2_rn(hi[4], hi[6]);
-                fh.z = pack_bf16x2_rn(hi[1], hi[3]);
-                fh.w = pack_bf16x2_rn(hi[5], hi[7]);
-                fl.x = pack_bf16x2_rn(lo[0], lo[2]);
-                fl.y = pack_bf16x2_rn(lo[4], lo[6]);
-                fl.z = pack_bf16x2_rn(lo[1], lo[3]);
-                fl.w = pack_bf16x2_rn(lo[5], lo[7]);
-                const int h = tok >> 3;
-                ent[(2 * h) * 32 + 4 * (tok & 7) + t] = fh;
-                ent[(2 * h + 1) * 32 + 4 * (tok & 7) + t] = fl;
-                if (t == 0) sm.xs[pb * M + tok] = su;
             }
             if (!fin && t == 0) *reinterpret_cast<volatile int *>(sm.flag) = 1;
         }
     }
 }
 
+// m >= 8: stage the CTA's slice of X as one fp16 term per element. A task is
+// one block of the slice for all tokens: lane 4 j + t holds token 8h + j's
+// elements 4t .. 4t+3 and 16 + 4t .. 19 + 4t, for each h. The warp agrees on
+// the block's scale 2^e, from the largest finite |x| of any token (it lands
+// in [1, 2)), and stores x * 2^-e rounded to fp16 (k-step 0: elements
+// (4t, 4t+2), (4t+1, 4t+3); k-step 1: those plus 16, divided by 16 to meet
+// weights of 16 (q - 8)) at lane 4 j + t of entry (p, b, h), which is the
+// lane that reads it. Every element keeps 11 significant bits (relative error
+// at most 2^-11) unless it lies 2^14 below the block's largest, and NaN and
+// infinity pass unchanged.
+template <int M>
+__device__ __forceinline__ void stage_x_wide(const DecodeArgs &a, const VSmem &sm, int p0, int P, int w, int lane)
+{
+    constexpr int H = M / 8;
+    constexpr int kBatch = 64 / M;                  // blocks per warp whose loads are in flight together
+    const int j = lane >> 2, t = lane & 3;
+    const int E = 2 * P;                            // blocks of the slice
+    int xrow[H];
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const int tok = 8 * h + j;
+        xrow[h] = tok < a.m ? (a.rows ? __ldg(a.rows + tok) : tok) : -1;
+    }
+    for (int e0 = w; e0 < E; e0 += kWarps * kBatch) {
+        float4 xa[kBatch][H], xb[kBatch][H];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int blk = 2 * p0 + e0 + kWarps * i;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                xa[i][h] = make_float4(0.f, 0.f, 0.f, 0.f);
+                xb[i][h] = xa[i][h];
+                if (e0 + kWarps * i < E && blk < a.nb && xrow[h] >= 0) {
+                    const float *xr = a.X + static_cast<int64_t>(xrow[h]) * a.ldx + 32 * blk + 4 * t;
+                    xa[i][h] = __ldg(reinterpret_cast<const float4 *>(xr));
+                    xb[i][h] = __ldg(reinterpret_cast<const float4 *>(xr + 16));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int pb = e0 + kWarps * i;         // 2p + b within the slice
+            if (pb >= E) break;                     // warp-uniform
+            unsigned mb = 0u;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                const float v[8] = {xa[i][h].x, xa[i][h].y, xa[i][h].z, xa[i][h].w,
+                                    xb[i][h].x, xb[i][h].y, xb[i][h].z, xb[i][h].w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const unsigned bits = __float_as_uint(v[q]) & 0x7FFFFFFFu;
+                    if (bits < 0x7F800000u) mb = max(mb, bits);
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+            int ex = 0;                             // largest finite |x| in [2^ex, 2^(ex + 1))
+            if (mb >= 0x00800000u) ex = min(static_cast<int>(mb >> 23) - 127, 126);
+            else if (mb != 0u) ex = -126;           // subnormal: scaled below 1
+            const float sd = __uint_as_float(static_cast<unsigned>(127 - ex) << 23);   // 2^-ex
+            const float sd16 = sd * 0.0625f;
+            uint4 *ent = sm.bimg + static_cast<size_t>(pb * H) * 32;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                uint4 f;
+                f.x = pack_half2_rn(xa[i][h].x * sd, xa[i][h].z * sd);
+                f.y = pack_half2_rn(xa[i][h].y * sd, xa[i][h].w * sd);
+                f.z = pack_half2_rn(xb[i][h].x * sd16, xb[i][h].z * sd16);
+                f.w = pack_half2_rn(xb[i][h].y * sd16, xb[i][h].w * sd16);
+                ent[h * 32 + lane] = f;
+            }
+            if (lane == 0) sm.xs[pb] = __uint_as_float(static_cast<unsigned>(127 + ex) << 23);   // 2^ex
+        }
+    }
+}
 
 // int8 weights: stage the CTA's slice of X (pairs p0 .. p0 + P - 1, 64
 // columns each) as fp16 B fragments. A task is one (pair, token): four lanes
@@ -476,8 +577,9 @@ __device__ __forceinline__ void stage_x_w8(const DecodeArgs &a, const VSmem &sm,
     }
 }
 
-// One record for all eight row tiles: y[rt][r][i] += row 16 rt + g + 8r's
-// part, for the token (and block, m <= 2) thread t holds:
+// One item (a record; for m >= 8 half of one) for all its row tiles:
+// y[rt][r][i] += the part of the item's row 16 rt + g + 8r for the token (and
+// block, m <= 2) thread t holds:
 //   m = 1:  token 0, block t of the record (t < 2; summed over t at the end);
 //   m = 2:  token t & 1, block t >> 1 (summed over t, t ^ 2 at the end);
 //   m = 4:  token t;
@@ -486,11 +588,14 @@ __device__ __forceinline__ void stage_x_w8(const DecodeArgs &a, const VSmem &sm,
 // `p` is the record's pair within the slice (its X entries).
 template <int M, bool EXACT>
 __device__ __forceinline__ void record_mma(const VSmem &sm, uint32_t rec, int p, int lane,
-                                           float (&y)[8][2][acc_width(M)])
+                                           float (&y)[item_tiles(M)][2][acc_width(M)])
 {
     constexpr int kNQ = entries_per_block(M);
     const int g = lane >> 2, t = lane & 3;
     const uint32_t bimg = smem_u32(sm.bimg) + static_cast<uint32_t>(p * 2 * kNQ * entry_bytes(M) + lane * 16);
+    // this lane's words of row g (nibbles) and its scale word; row tiles and
+    // the rows + 8 are compile-time offsets from these
+    const uint32_t bq = rec + static_cast<uint32_t>(16 * g + 4 * t), bs = rec + static_cast<uint32_t>(4 * g);
     if constexpr (M <= 2) {
         // one accumulator tile for both blocks: lanes outside a block's own
         // columns take zeros for its MMAs
@@ -500,109 +605,97 @@ __device__ __forceinline__ void record_mma(const VSmem &sm, uint32_t rec, int p,
                             static_cast<uint32_t>((p * 2 + (lane >> SH)) * entry_bytes(M) + (lane & (entry_lanes(M) - 1)) * 16);
         const uint4 B0 = (lane >> SH) == 0 ? ld128(bl) : zero;
         const uint4 B1 = (lane >> SH) == 1 ? ld128(bl) : zero;
-        // this thread's (block, token) column pair: corrections and 2^e
-        const int bt = M == 1 ? t : (t >> 1);
-        const bool live = M == 2 || t < 2;
-        const float4 *pp = sm.xp + ((p * 2 + (live ? bt : 0)) * M + (M == 1 ? 0 : (t & 1))) * 2;
-        const float4 cr = live ? ld128f(smem_u32(pp)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float su = live ? ld128f(smem_u32(pp + 1)).x : 0.f;
-#pragma unroll
-        for (int rt = 0; rt < 8; ++rt) {
-            const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
-            const uint32_t w00 = ld32(rec + kRecQs0Off + 16 * r0 + 4 * t);
-            const uint32_t w01 = ld32(rec + kRecQs0Off + 16 * r0 + 128 + 4 * t);
-            const uint32_t w10 = ld32(rec + kRecQs1Off + 16 * r0 + 4 * t);
-            const uint32_t w11 = ld32(rec + kRecQs1Off + 16 * r0 + 128 + 4 * t);
-            const uint32_t s0 = ld32(rec + kRecScaleOff + 4 * r0), s1 = ld32(rec + kRecScaleOff + 4 * r0 + 32);
+        // this thread's (block, token) column pair: corrections and 2^e (for
+        // m = 1, lanes t = 2, 3 hold columns without X and are never stored;
+        // they read block t & 1's)
+        const int bt = M == 1 ? (t & 1) : (t >> 1);
+        const float4 cr = ld128f(smem_u32(sm.xp + (p * 2 + bt) * M + (M == 1 ? 0 : (t & 1))));
+        const float su = cr.z;
+        const int sh = 16 * bt;                     // the block's half of a scale word
+        static_for<8>([&](auto RT) {
+            constexpr int rt = decltype(RT)::value;
+            const uint32_t w00 = ld32o<kRecQs0Off + 256 * rt>(bq), w01 = ld32o<kRecQs0Off + 256 * rt + 128>(bq);
+            const uint32_t w10 = ld32o<kRecQs1Off + 256 * rt>(bq), w11 = ld32o<kRecQs1Off + 256 * rt + 128>(bq);
+            const uint32_t s0 = ld32o<kRecScaleOff + 64 * rt>(bs), s1 = ld32o<kRecScaleOff + 64 * rt + 32>(bs);
             uint32_t a[2][2][4];                    // [block][k-step][fragment]
             weights_f16<EXACT>(w00, a[0][0][0], a[0][0][2], a[0][1][0], a[0][1][2]);
             weights_f16<EXACT>(w01, a[0][0][1], a[0][0][3], a[0][1][1], a[0][1][3]);
             weights_f16<EXACT>(w10, a[1][0][0], a[1][0][2], a[1][1][0], a[1][1][2]);
             weights_f16<EXACT>(w11, a[1][0][1], a[1][0][3], a[1][1][1], a[1][1][3]);
-            // k-step 0 (low nibbles) and k-step 1 (high nibbles) accumulate
-            // apart, each from its columns' corrections
+            // both k-steps of both blocks into one tile, from the columns'
+            // corrections
             float D[4] = {EXACT ? 0.f : cr.x, EXACT ? 0.f : cr.y, EXACT ? 0.f : cr.x, EXACT ? 0.f : cr.y};
-            float E[4] = {EXACT ? 0.f : cr.z, EXACT ? 0.f : cr.w, EXACT ? 0.f : cr.z, EXACT ? 0.f : cr.w};
             mma_acc_f16(D, a[0][0], B0.x, B0.y);
-            mma_acc_f16(E, a[0][1], B0.z, B0.w);
             mma_acc_f16(D, a[1][0], B1.x, B1.y);
-            mma_acc_f16(E, a[1][1], B1.z, B1.w);
-            const float d0 = live ? half_of(s0, bt) : 0.f;
-            const float d1 = live ? half_of(s1, bt) : 0.f;
+            mma_acc_f16(D, a[0][1], B0.z, B0.w);
+            mma_acc_f16(D, a[1][1], B1.z, B1.w);
+            const float d0 = half_at(s0, sh), d1 = half_at(s1, sh);
             // hi column + lo column (kept 2^8 larger)
-            y[rt][0][0] = fmaf(d0 * su, fmaf(D[1] + E[1], 0x1p-8f, D[0] + E[0]), y[rt][0][0]);
-            y[rt][1][0] = fmaf(d1 * su, fmaf(D[3] + E[3], 0x1p-8f, D[2] + E[2]), y[rt][1][0]);
-        }
+            y[rt][0][0] = fmaf(d0 * su, fmaf(D[1], 0x1p-8f, D[0]), y[rt][0][0]);
+            y[rt][1][0] = fmaf(d1 * su, fmaf(D[3], 0x1p-8f, D[2]), y[rt][1][0]);
+        });
     } else if constexpr (M == 4) {
         // a tile per block: thread t holds token t
         const uint4 B0 = ld128(bimg), B1 = ld128(bimg + 512);
-        const float4 c0 = ld128f(smem_u32(sm.xp + (p * 2 * 4 + t) * 2));
-        const float4 c1 = ld128f(smem_u32(sm.xp + ((p * 2 + 1) * 4 + t) * 2));
-        const float su0 = ld128f(smem_u32(sm.xp + (p * 2 * 4 + t) * 2 + 1)).x;
-        const float su1 = ld128f(smem_u32(sm.xp + ((p * 2 + 1) * 4 + t) * 2 + 1)).x;
-#pragma unroll
-        for (int rt = 0; rt < 8; ++rt) {
-            const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
-            const uint32_t w00 = ld32(rec + kRecQs0Off + 16 * r0 + 4 * t);
-            const uint32_t w01 = ld32(rec + kRecQs0Off + 16 * r0 + 128 + 4 * t);
-            const uint32_t w10 = ld32(rec + kRecQs1Off + 16 * r0 + 4 * t);
-            const uint32_t w11 = ld32(rec + kRecQs1Off + 16 * r0 + 128 + 4 * t);
-            const uint32_t s0 = ld32(rec + kRecScaleOff + 4 * r0), s1 = ld32(rec + kRecScaleOff + 4 * r0 + 32);
+        const float4 c0 = ld128f(smem_u32(sm.xp + p * 2 * 4 + t));
+        const float4 c1 = ld128f(smem_u32(sm.xp + (p * 2 + 1) * 4 + t));
+        const float su0 = c0.z, su1 = c1.z;
+        static_for<8>([&](auto RT) {
+            constexpr int rt = decltype(RT)::value;
+            const uint32_t w00 = ld32o<kRecQs0Off + 256 * rt>(bq), w01 = ld32o<kRecQs0Off + 256 * rt + 128>(bq);
+            const uint32_t w10 = ld32o<kRecQs1Off + 256 * rt>(bq), w11 = ld32o<kRecQs1Off + 256 * rt + 128>(bq);
+            const uint32_t s0 = ld32o<kRecScaleOff + 64 * rt>(bs), s1 = ld32o<kRecScaleOff + 64 * rt + 32>(bs);
             uint32_t a[2][2][4];
             weights_f16<EXACT>(w00, a[0][0][0], a[0][0][2], a[0][1][0], a[0][1][2]);
             weights_f16<EXACT>(w01, a[0][0][1], a[0][0][3], a[0][1][1], a[0][1][3]);
             weights_f16<EXACT>(w10, a[1][0][0], a[1][0][2], a[1][1][0], a[1][1][2]);
             weights_f16<EXACT>(w11, a[1][0][1], a[1][0][3], a[1][1][1], a[1][1][3]);
             float D0[4] = {EXACT ? 0.f : c0.x, EXACT ? 0.f : c0.y, EXACT ? 0.f : c0.x, EXACT ? 0.f : c0.y};
-            float E0[4] = {EXACT ? 0.f : c0.z, EXACT ? 0.f : c0.w, EXACT ? 0.f : c0.z, EXACT ? 0.f : c0.w};
             float D1[4] = {EXACT ? 0.f : c1.x, EXACT ? 0.f : c1.y, EXACT ? 0.f : c1.x, EXACT ? 0.f : c1.y};
-            float E1[4] = {EXACT ? 0.f : c1.z, EXACT ? 0.f : c1.w, EXACT ? 0.f : c1.z, EXACT ? 0.f : c1.w};
             mma_acc_f16(D0, a[0][0], B0.x, B0.y);
             mma_acc_f16(D1, a[1][0], B1.x, B1.y);
-            mma_acc_f16(E0, a[0][1], B0.z, B0.w);
-            mma_acc_f16(E1, a[1][1], B1.z, B1.w);
-            y[rt][0][0] = fmaf(half_of(s0, 0) * su0, fmaf(D0[1] + E0[1], 0x1p-8f, D0[0] + E0[0]), y[rt][0][0]);
-            y[rt][1][0] = fmaf(half_of(s1, 0) * su0, fmaf(D0[3] + E0[3], 0x1p-8f, D0[2] + E0[2]), y[rt][1][0]);
-            y[rt][0][0] = fmaf(half_of(s0, 1) * su1, fmaf(D1[1] + E1[1], 0x1p-8f, D1[0] + E1[0]), y[rt][0][0]);
-            y[rt][1][0] = fmaf(half_of(s1, 1) * su1, fmaf(D1[3] + E1[3], 0x1p-8f, D1[2] + E1[2]), y[rt][1][0]);
-        }
+            mma_acc_f16(D0, a[0][1], B0.z, B0.w);
+            mma_acc_f16(D1, a[1][1], B1.z, B1.w);
+            y[rt][0][0] = fmaf(half_of(s0, 0) * su0, fmaf(D0[1], 0x1p-8f, D0[0]), y[rt][0][0]);
+            y[rt][1][0] = fmaf(half_of(s1, 0) * su0, fmaf(D0[3], 0x1p-8f, D0[2]), y[rt][1][0]);
+            y[rt][0][0] = fmaf(half_of(s0, 1) * su1, fmaf(D1[1], 0x1p-8f, D1[0]), y[rt][0][0]);
+            y[rt][1][0] = fmaf(half_of(s1, 1) * su1, fmaf(D1[3], 0x1p-8f, D1[2]), y[rt][1][0]);
+        });
     } else {
-        // tiles (block b, half h): tokens 8h .. 8h + 7; hi and lo are two MMAs
+        // a half record (64 rows, scales and nibbles at 0, 256 and 1280);
+        // tiles (block b, tokens 8h .. 8h + 7): exact weights q - 8 (k-step 0)
+        // and 16 (q - 8) (k-step 1) against the block's single fp16 term
         constexpr int H = M / 8;
-        float2 su[2][H];
+        uint4 B[2][H];
 #pragma unroll
         for (int b = 0; b < 2; ++b)
 #pragma unroll
-            for (int h = 0; h < H; ++h) su[b][h] = ld64f(smem_u32(sm.xs + (p * 2 + b) * M + 8 * h + 2 * t));
-#pragma unroll
-        for (int rt = 0; rt < 8; ++rt) {
-            const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
-            const uint32_t s0 = ld32(rec + kRecScaleOff + 4 * r0), s1 = ld32(rec + kRecScaleOff + 4 * r0 + 32);
+            for (int h = 0; h < H; ++h) B[b][h] = ld128(bimg + static_cast<uint32_t>((b * H + h) * 512));
+        const float2 su = ld64f(smem_u32(sm.xs + 2 * p));   // 2^e of blocks 0 and 1
+        static_for<item_tiles(M)>([&](auto RT) {
+            constexpr int rt = decltype(RT)::value;
+            const uint32_t w00 = ld32o<kHalfQs0Off + 256 * rt>(bq), w01 = ld32o<kHalfQs0Off + 256 * rt + 128>(bq);
+            const uint32_t w10 = ld32o<kHalfQs1Off + 256 * rt>(bq), w11 = ld32o<kHalfQs1Off + 256 * rt + 128>(bq);
+            const uint32_t s0 = ld32o<64 * rt>(bs), s1 = ld32o<64 * rt + 32>(bs);
+            uint32_t a[2][2][4];
+            weights_f16<true>(w00, a[0][0][0], a[0][0][2], a[0][1][0], a[0][1][2]);
+            weights_f16<true>(w01, a[0][0][1], a[0][0][3], a[0][1][1], a[0][1][3]);
+            weights_f16<true>(w10, a[1][0][0], a[1][0][2], a[1][1][0], a[1][1][2]);
+            weights_f16<true>(w11, a[1][0][1], a[1][0][3], a[1][1][1], a[1][1][3]);
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                const uint32_t qo = b ? kRecQs1Off : kRecQs0Off;
-                const uint32_t w0 = ld32(rec + qo + 16 * r0 + 4 * t), w1 = ld32(rec + qo + 16 * r0 + 128 + 4 * t);
-                uint32_t v0[4], v1[4];
-                weights_of<true>(w0, v0);
-                weights_of<true>(w1, v1);
-                const uint32_t A0[4] = {v0[0], v1[0], v0[1], v1[1]}, A1[4] = {v0[2], v1[2], v0[3], v1[3]};
-                const float dg = half_of(s0, b), dg8 = half_of(s1, b);
+                const float sb = b ? su.y : su.x;
+                const float ds0 = half_of(s0, b) * sb, ds1 = half_of(s1, b) * sb;
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    const uint4 Bh = ld128(bimg + static_cast<uint32_t>((b * kNQ + 2 * h) * 512));
-                    const uint4 Bl = ld128(bimg + static_cast<uint32_t>((b * kNQ + 2 * h + 1) * 512));
-                    float D[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_acc(D, A0, Bh.x, Bh.y);
-                    mma_acc(D, A1, Bh.z, Bh.w);
-                    mma_acc(D, A0, Bl.x, Bl.y);
-                    mma_acc(D, A1, Bl.z, Bl.w);
-                    y[rt][0][2 * h] = fmaf(dg * su[b][h].x, D[0], y[rt][0][2 * h]);
-                    y[rt][0][2 * h + 1] = fmaf(dg * su[b][h].y, D[1], y[rt][0][2 * h + 1]);
-                    y[rt][1][2 * h] = fmaf(dg8 * su[b][h].x, D[2], y[rt][1][2 * h]);
-                    y[rt][1][2 * h + 1] = fmaf(dg8 * su[b][h].y, D[3], y[rt][1][2 * h + 1]);
+                    float D[4];
+                    mma_f16(D, a[b][0], B[b][h].x, B[b][h].y);
+                    mma_acc_f16(D, a[b][1], B[b][h].z, B[b][h].w);
+                    fma2(y[rt][0][2 * h], y[rt][0][2 * h + 1], D[0], D[1], ds0);
+                    fma2(y[rt][1][2 * h], y[rt][1][2 * h + 1], D[2], D[3], ds1);
                 }
             }
-        }
+        });
     }
 }
 
@@ -618,24 +711,25 @@ __device__ __forceinline__ void codes_f16(uint32_t w, uint32_t &even, uint32_t &
     odd = hsub2_bits(o, 0x64806480u);
 }
 
-// One int8 record for all eight row tiles: y[rt][r][i] += 2^-e * (row's
+// One int8 item (a record; for m >= 8 its 64-row half) for all its row tiles:
+// y[rt][r][i] += 2^-e * (row's
 // codes . X's pair), for the token thread t holds (m <= 4: token t; m = 8:
 // 2t + i; m = 16: 8 (i >> 1) + 2t + (i & 1)); the row's scale comes when Y is
 // written.
 template <int M>
 __device__ __forceinline__ void record_mma_w8(const VSmem &sm, uint32_t rec, int p, int lane,
-                                              float (&y)[8][2][acc_width(M)])
+                                              float (&y)[item_tiles(M)][2][acc_width(M)])
 {
     constexpr int kNE = w8_entries(M);
     const int g = lane >> 2, t = lane & 3;
     const uint32_t bimg = smem_u32(sm.bimg) + static_cast<uint32_t>(p * xfrag_bytes(M, kFmtW8) + lane * 32);
+    const uint32_t bq = rec + static_cast<uint32_t>(kPairK * g + 16 * t);   // row g's 16 codes of this lane
     if constexpr (M <= 4) {
         const uint4 e0 = ld128(bimg), e1 = ld128(bimg + 16);
         const float su = t < M ? sm.xs[p * M + t] : 0.f;
-#pragma unroll
-        for (int rt = 0; rt < 8; ++rt) {
-            const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
-            const uint4 qa = ld128(rec + r0 * kPairK + 16 * t), qb = ld128(rec + (r0 + 8) * kPairK + 16 * t);
+        static_for<item_tiles(M)>([&](auto RT) {
+            constexpr int rt = decltype(RT)::value;
+            const uint4 qa = ld128o<1024 * rt>(bq), qb = ld128o<1024 * rt + 512>(bq);
             const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
             float D[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
             const uint32_t bx[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
@@ -650,16 +744,15 @@ __device__ __forceinline__ void record_mma_w8(const VSmem &sm, uint32_t rec, int
             }
             y[rt][0][0] = fmaf(su, (D[0] + E[0]) + (D[1] + E[1]), y[rt][0][0]);
             y[rt][1][0] = fmaf(su, (D[2] + E[2]) + (D[3] + E[3]), y[rt][1][0]);
-        }
+        });
     } else {
         constexpr int H = M / 8;
         float2 su[H];
 #pragma unroll
         for (int h = 0; h < H; ++h) su[h] = ld64f(smem_u32(sm.xs + p * M + 8 * h + 2 * t));
-#pragma unroll
-        for (int rt = 0; rt < 8; ++rt) {
-            const uint32_t r0 = static_cast<uint32_t>(16 * rt + g);
-            const uint4 qa = ld128(rec + r0 * kPairK + 16 * t), qb = ld128(rec + (r0 + 8) * kPairK + 16 * t);
+        static_for<item_tiles(M)>([&](auto RT) {
+            constexpr int rt = decltype(RT)::value;
+            const uint4 qa = ld128o<1024 * rt>(bq), qb = ld128o<1024 * rt + 512>(bq);
             const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
             uint32_t A[4][4];
 #pragma unroll
@@ -686,7 +779,7 @@ __device__ __forceinline__ void record_mma_w8(const VSmem &sm, uint32_t rec, int
                 y[rt][1][2 * h] = fmaf(su[h].x, D[2], y[rt][1][2 * h]);
                 y[rt][1][2 * h + 1] = fmaf(su[h].y, D[3], y[rt][1][2 * h + 1]);
             }
-        }
+        });
     }
     (void)kNE;
 }
@@ -701,31 +794,44 @@ __device__ __forceinline__ int acc_token(int t, int i)
     else return 8 * (i >> 1) + 2 * t + (i & 1);
 }
 
-// Store this warp's partial rows of a group (all 128 rows) into part[tb][c]
-// ([M][128] floats).
+// This warp's partial rows of buffer tb.
+__device__ __forceinline__ float *part_of(const VSmem &sm, int tb, int c, int M)
+{
+    if (sm.part_in_ring) {
+        // the warp's first ring slot
+        const int first = halves(M) == 2 ? (c >> 2) * sm.rh + (c & 3) : c;
+        return sm.part + static_cast<size_t>(first) * sm.part_stride;
+    }
+    return sm.part + static_cast<size_t>(tb * kWarps + c) * sm.part_stride;
+}
+
+// Store this warp's partial rows of a group (the item rows of its half,
+// [M][item_rows] floats) into buffer tb.
 template <int M>
-__device__ __forceinline__ void store_partials(const VSmem &sm, int tb, int c, int lane, float (&y)[8][2][acc_width(M)])
+__device__ __forceinline__ void store_partials(const VSmem &sm, int tb, int c, int lane,
+                                               float (&y)[item_tiles(M)][2][acc_width(M)])
 {
     constexpr int NY = acc_width(M);
+    constexpr int RI = item_rows(M);
     const int g = lane >> 2, t = lane & 3;
     // m = 1: blocks 0 and 1 of a row sit in threads t = 0, 1; m = 2: blocks
     // 0 and 1 of a token in threads t and t ^ 2
 #pragma unroll
-    for (int rt = 0; rt < 8; ++rt)
+    for (int rt = 0; rt < item_tiles(M); ++rt)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             if constexpr (M == 1) y[rt][r][0] += __shfl_xor_sync(0xFFFFFFFFu, y[rt][r][0], 1);
             if constexpr (M == 2) y[rt][r][0] += __shfl_xor_sync(0xFFFFFFFFu, y[rt][r][0], 2);
         }
     const bool writes = M == 1 ? t == 0 : (M == 2 ? t < 2 : true);
-    float *pp = sm.part + static_cast<size_t>(tb * kWarps + c) * sm.part_stride;
+    float *pp = part_of(sm, tb, c, M);
     if (writes)
 #pragma unroll
-        for (int rt = 0; rt < 8; ++rt)
+        for (int rt = 0; rt < item_tiles(M); ++rt)
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int i = 0; i < NY; ++i) pp[acc_token<M>(t, i) * kGroupRows + 16 * rt + g + 8 * r] = y[rt][r][i];
+                for (int i = 0; i < NY; ++i) pp[acc_token<M>(t, i) * RI + 16 * rt + g + 8 * r] = y[rt][r][i];
 }
 
 // Rows of a warp's slice in the reduction: lane l handles row 16c + (l & 15)
@@ -736,12 +842,15 @@ struct SliceRows {
     float v[NT];
 };
 
-// Sum the eight warps' partials of a group (buffer tb) for this warp's rows,
-// in warp order.
+// Sum the partials of a group (buffer tb) for this warp's rows, in warp
+// order: the eight warps' (m <= 4), or the four warps' of this half (m >= 8).
 template <int M>
 __device__ __forceinline__ void sum_partials(const VSmem &sm, int tb, int c, int lane, SliceRows<M> &s)
 {
-    const int row = c * kSliceRows + (lane & (kSliceRows - 1));
+    constexpr int RI = item_rows(M);
+    constexpr int NW = kWarps / halves(M);
+    const int row = (c * kSliceRows) % RI + (lane & (kSliceRows - 1));   // within the half
+    const int w0 = halves(M) == 2 ? (c >> 2) * NW : 0;
     const int t0 = lane >> 4;
 #pragma unroll
     for (int h = 0; h < SliceRows<M>::NT; ++h) {
@@ -749,7 +858,7 @@ __device__ __forceinline__ void sum_partials(const VSmem &sm, int tb, int c, int
         float v = 0.0f;
         if (tok < M)
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += sm.part[static_cast<size_t>(tb * kWarps + w) * sm.part_stride + tok * kGroupRows + row];
+            for (int w = 0; w < NW; ++w) v += part_of(sm, tb, w0 + w, M)[tok * RI + row];
         s.v[h] = v;
     }
 }
@@ -823,52 +932,71 @@ __device__ __forceinline__ bool reduce_group(const DecodeArgs &a, const VSmem &s
     return true;
 }
 
-// Issue the bulk copy of the CTA's record n (group n / P, pair n % P of its
-// slice) into ring slot s. Lane 0 of the slot's warp only.
-template <int F>
-__device__ __forceinline__ void load_record(const DecodeArgs &a, const VSmem &sm, int n, int P, int s, int G0, int p0,
-                                            uint64_t pol)
+// Issue the copy of the item of group gi, pair j of the CTA's slice (the
+// whole record, or rows 64 hf .. 64 hf + 63 of it) into ring slot s. Lane 0
+// of the slot's warp only.
+template <int M, int F>
+__device__ __forceinline__ void load_item(const DecodeArgs &a, const VSmem &sm, int gi, int j, int hf, int s, int G0,
+                                          int p0, uint64_t pol)
 {
-    constexpr int kRB = rec_bytes(F);
-    const int gi = n / P, j = n - gi * P;
+    constexpr int kRB = rec_bytes(F), kSB = slot_bytes(M, F);
     const int64_t rec = static_cast<int64_t>(G0 + gi * a.clusters) * a.np + p0 + j;
-    mbar_arrive_expect_tx(&sm.full[s], kRB);
-    bulk_g2s_hint(sm.ring + static_cast<size_t>(s) * kRB, a.W + rec * kRB, kRB, &sm.full[s], pol);
+    const uint8_t *src = a.W + rec * kRB;
+    uint8_t *dst = sm.ring + static_cast<size_t>(s) * kSB;
+    mbar_arrive_expect_tx(&sm.full[s], kSB);
+    if constexpr (halves(M) == 1) {
+        bulk_g2s_hint(dst, src, kRB, &sm.full[s], pol);
+    } else if constexpr (F == kFmtW8) {
+        bulk_g2s_hint(dst, src + hf * kSB, kSB, &sm.full[s], pol);
+    } else {
+        // the half's scales and the nibbles of its rows in either block
+        bulk_g2s_hint(dst, src + kRecScaleOff + 256 * hf, 256, &sm.full[s], pol);
+        bulk_g2s_hint(dst + kHalfQs0Off, src + kRecQs0Off + 1024 * hf, 1024, &sm.full[s], pol);
+        bulk_g2s_hint(dst + kHalfQs1Off, src + kRecQs1Off + 1024 * hf, 1024, &sm.full[s], pol);
+    }
 }
 
-// The warp's records, group by group: products into registers, partial rows
+// The warp's items, group by group: products into registers, partial rows
 // into shared memory at each group's end, the previous group's reduction.
-// `pending` tracks the warp's first record not yet read (for the drain after
-// a failure).
+// Warp c takes items c, c + 8, ... of the CTA's sequence (m >= 8: warp c of
+// half c / 4 takes items c % 4, c % 4 + 4, ... of that half's sequence) and
+// their ring slots. `pending` tracks the warp's first item not yet read (for
+// the drain after a failure).
 template <int M, bool EXACT, int F>
 __device__ __forceinline__ bool consume(const DecodeArgs &a, const VSmem &sm, int c, int lane, int rank, int G0, int p0,
                                         int P, int ntiles, bool merged, uint64_t pol, int &pending,
                                         SliceRows<M> &keep)
 {
-    constexpr int NY = acc_width(M);
-    const int R = a.ring;
+    constexpr int NY = acc_width(M), KT = item_tiles(M), NS = kWarps / halves(M);
+    const int hf = c / NS, cs = c % NS;
+    const int RH = sm.rh;
     const int total = ntiles * P;
     const uint32_t ring0 = smem_u32(sm.ring);
-    int n = c;                                        // the warp's next record
+    int n = cs;                                       // the warp's next item
+    int sl = cs, ph = 0;                              // its slot within the half's ring, the slot's parity
+    int fg = (cs + RH) / P, fj = cs + RH - fg * P;    // group and pair of the item RH ahead (the refill)
     for (int g = 0; g < ntiles; ++g) {
-        float y[8][2][NY];
+        float y[KT][2][NY];
 #pragma unroll
-        for (int rt = 0; rt < 8; ++rt)
+        for (int rt = 0; rt < KT; ++rt)
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
                 for (int i = 0; i < NY; ++i) y[rt][r][i] = 0.f;
-        for (; n < (g + 1) * P; n += kWarps) {
-            const int s = n % R;
-            if (!warp_wait(&sm.full[s], static_cast<uint32_t>((n / R) & 1), a.wait_ns)) return false;
-            const uint32_t rec = ring0 + static_cast<uint32_t>(s * rec_bytes(F));
+        for (; n < (g + 1) * P; n += NS) {
+            const int s = hf * RH + sl;
+            if (!warp_wait(&sm.full[s], static_cast<uint32_t>(ph), a.wait_ns)) return false;
+            const uint32_t rec = ring0 + static_cast<uint32_t>(s * slot_bytes(M, F));
             if constexpr (F == kFmtW8) record_mma_w8<M>(sm, rec, n - g * P, lane, y);
             else record_mma<M, EXACT>(sm, rec, n - g * P, lane, y);
-            // the record's MMAs, which consume its loads, are issued: refill
-            // the slot with the record R places ahead (same warp)
+            // the item's MMAs, which consume its loads, are issued: refill
+            // the slot with the item RH places ahead (same warp)
             __syncwarp();
-            if (lane == 0 && n + R < total) load_record<F>(a, sm, n + R, P, s, G0, p0, pol);
-            pending = n + kWarps;
+            if (lane == 0 && n + RH < total) load_item<M, F>(a, sm, fg, fj, hf, s, G0, p0, pol);
+            pending = n + NS;
+            for (fj += NS; fj >= P; fj -= P) ++fg;
+            sl += NS;
+            if (sl >= RH) sl -= RH, ph ^= 1;
         }
         const int tb = g & 1;
         if (g >= 2 && !warp_wait(&sm.gfree[tb], static_cast<uint32_t>(((g >> 1) & 1) ^ 1), a.wait_ns)) return false;
@@ -881,11 +1009,11 @@ __device__ __forceinline__ bool consume(const DecodeArgs &a, const VSmem &sm, in
 }
 
 template <int M, int F>
-__global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const DecodeArgs call, const ExpertSet set)
+__global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const DecodeArgs call, const ExpertSet set)
 {
-    constexpr int kRB = rec_bytes(F);
+    constexpr int kSB = slot_bytes(M, F);
+    constexpr int NS = kWarps / halves(M);
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    constexpr int kNQ = entries_per_block(M);
     const int tid = threadIdx.x, c = tid >> 5, lane = tid & 31;
     const int S = call.S;
     const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -906,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
     const int ntiles = G0 < a.groups ? (a.groups - 1 - G0) / a.clusters + 1 : 0;
     const int p0 = rank * a.pbase + min(rank, a.prem);
     const int P = a.pbase + (rank < a.prem ? 1 : 0);
-    const int total = ntiles * P;                   // records this CTA streams
+    const int total = ntiles * P;                   // items of each half's sequence
     const int R = a.ring;
     // Every CTA of the cluster lays out its shared memory for the largest
     // slice, so that a barrier or a row buffer sits at the same offset in all
@@ -917,18 +1045,21 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
 
     VSmem sm;
     sm.ring = smem_raw;
-    sm.bimg = reinterpret_cast<uint4 *>(sm.ring + static_cast<size_t>(R) * kRB);
-    uint8_t *after_b = sm.ring + static_cast<size_t>(R) * kRB + static_cast<size_t>(Pmax) * xfrag_bytes(M, F);
+    sm.rh = R / halves(M);
+    sm.bimg = reinterpret_cast<uint4 *>(sm.ring + static_cast<size_t>(R) * kSB);
+    uint8_t *after_b = sm.ring + static_cast<size_t>(R) * kSB + static_cast<size_t>(Pmax) * xfrag_bytes(M, F);
     sm.xp = reinterpret_cast<float4 *>(after_b);
     sm.xs = reinterpret_cast<float *>(after_b);
     float *after_x = reinterpret_cast<float *>(after_b + xparam_region(M, F, Pmax));
     // With a single group per CTA and the whole slice in the ring (no slot is
     // refilled), warp c's partial rows go into its first ring slot, which it
     // has read by then.
-    const bool part_in_ring = a.groups <= a.clusters && R >= Pmax && R >= kWarps && M * kGroupRows * 4 <= kRB;
+    const bool part_in_ring =
+        a.groups <= a.clusters && sm.rh >= Pmax && sm.rh >= NS && M * item_rows(M) * 4 <= kSB;
+    sm.part_in_ring = part_in_ring;
     sm.part = part_in_ring ? reinterpret_cast<float *>(sm.ring) : after_x;
-    sm.red = after_x + (part_in_ring ? 0 : static_cast<size_t>(NB) * kWarps * M * kGroupRows);
-    sm.part_stride = part_in_ring ? kRB / 4 : M * kGroupRows;
+    sm.red = after_x + (part_in_ring ? 0 : static_cast<size_t>(NB) * kWarps * M * item_rows(M));
+    sm.part_stride = part_in_ring ? kSB / 4 : M * item_rows(M);
     const int red_floats = S > 1 ? (merged ? 1 : 2) * (S - 1) * M * kGroupRows : 0;
     sm.flag = reinterpret_cast<int *>(sm.red + red_floats);
     sm.full = reinterpret_cast<uint64_t *>(sm.flag + 4);
@@ -967,14 +1098,16 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
     const uint64_t pol = policy_evict_first();
     if (!a.prefetch_w) pdl_wait();
     if (lane == 0)
-        for (int n = c; n < R && n < total; n += kWarps) load_record<F>(a, sm, n, P, n, G0, p0, pol);
+        for (int n = c % NS; n < sm.rh && n < total; n += NS)
+            load_item<M, F>(a, sm, n / P, n % P, c / NS, (c / NS) * sm.rh + n, G0, p0, pol);
     __syncwarp();
     pdl_wait();                                       // X, Y and the slot rows are the preceding kernel's
     if constexpr (F == kFmtW8) stage_x_w8<M>(a, sm, p0, P, c, lane);
+    else if constexpr (M >= 8) stage_x_wide<M>(a, sm, p0, P, c, lane);
     else stage_x<M>(a, sm, p0, P, c, lane);
     __syncthreads();
 
-    int pending = c;                                  // the warp's first record not yet read
+    int pending = c % NS;                             // the warp's first item not yet read
     SliceRows<M> keep;
 #pragma unroll
     for (int h = 0; h < SliceRows<M>::NT; ++h) keep.v[h] = 0.f;
@@ -988,8 +1121,9 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
         // A warp that gave up may still have copies landing in its slots
         // (the records after the last one it read): wait for them, bounded,
         // so that none lands after the CTA has exited.
-        for (int n = pending; n < total && n < pending + R; n += kWarps)
-            if (!warp_wait(&sm.full[n % R], static_cast<uint32_t>((n / R) & 1), a.wait_ns)) break;
+        for (int n = pending; n < total && n < pending + sm.rh; n += NS)
+            if (!warp_wait(&sm.full[(c / NS) * sm.rh + n % sm.rh], static_cast<uint32_t>((n / sm.rh) & 1), a.wait_ns))
+                break;
     }
 
     if (merged) {
@@ -1033,11 +1167,13 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
 // partial rows and the slices' rows are then double-buffered).
 size_t matvec_smem(int M, int F, int Pmax, int S, int ring, int parts)
 {
-    const bool part_in_ring = parts == 1 && ring >= Pmax && ring >= kWarps && M * kGroupRows * 4 <= rec_bytes(F);
-    size_t b = static_cast<size_t>(ring) * rec_bytes(F);
+    const int rh = ring / halves(M);
+    const bool part_in_ring =
+        parts == 1 && rh >= Pmax && rh >= kWarps / halves(M) && M * item_rows(M) * 4 <= slot_bytes(M, F);
+    size_t b = static_cast<size_t>(ring) * slot_bytes(M, F);
     b += static_cast<size_t>(Pmax) * xfrag_bytes(M, F);
     b += static_cast<size_t>(xparam_region(M, F, Pmax));
-    b += part_in_ring ? 0 : static_cast<size_t>(parts) * kWarps * M * kGroupRows * 4;
+    b += part_in_ring ? 0 : static_cast<size_t>(parts) * kWarps * M * item_rows(M) * 4;
     b += S > 1 ? static_cast<size_t>(parts * (S - 1)) * M * kGroupRows * 4 : 0;
     b += 16;                                                  // flag
     b += static_cast<size_t>(ring + 4 + 4 * kWarps + 1) * 8;  // barriers
@@ -1051,8 +1187,9 @@ template <int F>
 const void *matvec_fn_f(int M)
 {
     switch (M) {
-    case 1: return reinterpret_cast<const void *>(&matvec_kernel<1, F>);
-    case 2: return reinterpret_cast<const void *>(&matvec_kernel<2, F>);
+    // (int8 weights run the four-token instance from m = 1)
+    case 1: return reinterpret_cast<const void *>(&matvec_kernel<F == kFmtW8 ? 4 : 1, F>);
+    case 2: return reinterpret_cast<const void *>(&matvec_kernel<F == kFmtW8 ? 4 : 2, F>);
     case 4: return reinterpret_cast<const void *>(&matvec_kernel<4, F>);
     case 8: return reinterpret_cast<const void *>(&matvec_kernel<8, F>);
     default: return reinterpret_cast<const void *>(&matvec_kernel<16, F>);
@@ -1098,25 +1235,25 @@ int matvec_max_clusters(int M, int F, int S, size_t smem)
     return n;
 }
 
-// Issue cost of a record relative to one SM's share of HBM time for it
-// (first estimates from the source's instruction counts; the planner only
-// compares plans).
-double record_cost(int M) { return M <= 2 ? 0.5 : M == 4 ? 0.6 : M == 8 ? 0.9 : 1.6; }
+// Issue time of one record (Q4_0 bytes) on an SM running one CTA, in
+// microseconds: fitted to graph-replay timings of this kernel on GB300.
+double record_us(int M) { return M <= 1 ? 0.115 : M == 2 ? 0.13 : M == 4 ? 0.195 : M == 8 ? 0.206 : 0.291; }
 
 } // namespace
 
 // Choose the cluster size S (K slices per 128-row group), the number of
-// persistent clusters and the ring depth (records, a multiple of 8). For each
-// S: the deepest ring that fits one CTA's shared memory and the deepest that
-// leaves room for a second CTA on the SM (the next call's), neither deeper
-// than the CTA's records. The number of clusters is capped by what the
-// device holds at once (a second wave would double the time). Cost, in
-// record times of one SM's share of HBM: the busiest warp's records (the
-// CTA's records are dealt to its eight warps in turn) at the kernel's issue
-// cost, or the whole layer's stream if that is longer; the records a CTA
-// must wait for beyond its ring; the slices' reduction; per-group handshakes
-// of CTAs with several groups; and the start-up that cannot overlap the
-// preceding call when no SM has room for the next call's CTA.
+// persistent clusters and the ring depth (slots; the whole slice, or a
+// multiple of 8). Candidates: every S and depth whose shared memory fits,
+// with as many clusters as the device holds at once (up to one per group).
+// Their time is estimated in microseconds from constants fitted to graph-
+// replay timings of this kernel on GB300:
+//   the busiest SM's records at the kernel's issue time per record (two CTAs
+//   of one call on an SM hide each other's latencies), or the layer's HBM
+//   stream if longer, slowed when a refilled ring keeps too few bytes in
+//   flight per SM; a fixed start; X staging in rounds of loads; the slices'
+//   exchange; per-group handshakes of CTAs with several groups; and the
+//   start-up that cannot overlap the preceding call when no SM has room for
+//   the next call's CTA.
 bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan, int fmt)
 {
     if (m < 1 || m > 16 || sm_count < 1) return false;
@@ -1124,62 +1261,61 @@ bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan
     // int8 weights stage all four token columns of a tile (m <= 4 share the
     // four-token instance)
     const int M = F == kFmtW8 ? std::max(4, instance_of(m)) : instance_of(m);
-    // a record's weight bytes in units of a Q4_0 record
-    const double rw = static_cast<double>(rec_bytes(F)) / kRecordBytes;
+    const int hv = halves(M);
     const int64_t groups = ceil_div(n, kGroupRows);
     const int64_t np = ceil_div(k, kPairK);
-    const double total = static_cast<double>(groups * np);
     const size_t half = kSmemPerSM / 2 - 1024;
-    const double rc = record_cost(M);
+    const double rec_t = record_us(M) * rec_bytes(F) / kRecordBytes;
+    const double sm_bw = 6.77e6 / 152.0;                     // bytes per microsecond per SM
+    const double hbm_t = static_cast<double>(groups * np) * rec_bytes(F) / (sm_bw * sm_count);
     MatvecPlan best;
     double best_cost = 1e300;
     for (int S = 1; S <= kMaxSlices && S <= np; ++S) {
         const int64_t P = ceil_div(np, S);
-        for (int two = 0; two <= 1; ++two) {
-            const size_t limit = two ? half : kSmemOptIn;
-            // the cluster count decides the partial-row buffers: ask with one
-            const size_t probe = matvec_smem(M, F, static_cast<int>(P), S, kWarps, 1);
-            if (probe > limit) continue;
-            const int64_t cmax = matvec_max_clusters(M, F, S, probe);
-            if (cmax < 1) continue;
-            const int64_t clusters = std::min<int64_t>(groups, cmax);
-            const int64_t tiles = ceil_div(groups, clusters);
-            const int parts = tiles > 1 ? 2 : 1;
-            // the whole slice in the ring when it fits (no slot is refilled;
-            // any depth from 8), else the deepest multiple of 8 that fits
-            const int64_t recs_cta = tiles * P;
-            int ring = 0;
-            if (recs_cta <= kMaxRing) {
-                const int r = static_cast<int>(std::max<int64_t>(kWarps, recs_cta));
-                if (matvec_smem(M, F, static_cast<int>(P), S, r, parts) <= limit) ring = r;
-            }
-            for (int64_t r = std::min<int64_t>(kMaxRing, recs_cta / kWarps * kWarps); r >= kWarps && ring == 0; r -= kWarps)
-                if (matvec_smem(M, F, static_cast<int>(P), S, static_cast<int>(r), parts) <= limit)
-                    ring = static_cast<int>(r);
-            if (ring == 0) continue;
-            const size_t smem = matvec_smem(M, F, static_cast<int>(P), S, ring, parts);
-            if (matvec_max_clusters(M, F, S, smem) < clusters) continue;
-            const bool two_fit = smem <= half;
-            if (!two && two_fit) continue;             // the same plan as two = 1
-            const int64_t ctas = clusters * S;
-            const int per_sm = static_cast<int>(ceil_div(ctas, sm_count));
-            const double recs = static_cast<double>(tiles * P);
-            const double warp = static_cast<double>(ceil_div(tiles * P, kWarps)) * rc * 8.0 * per_sm / 4.0;
-            const double work = std::max(warp, rw * total / sm_count);
-            const double starve = recs > ring ? (recs - ring) * 0.5 : 0.0;
-            const double slices = S > 1 ? 3.0 + 1.0 * (S - 2) : 0.0;
-            const double groups_cost = tiles > 1 ? static_cast<double>(tiles) * (2.0 + 1.5 * S) : 0.0;
-            const double no_overlap = (!two_fit || per_sm > 1) ? 30.0 : 0.0;
-            const double cost = work + starve + slices + groups_cost + no_overlap;
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
-                best.M = M;
-                best.fmt = fmt;
-                best.S = S;
-                best.clusters = static_cast<int>(clusters);
-                best.ctas = static_cast<int>(ctas);
-                best.ring = ring;
-                best.smem = smem;
+        for (int parts = 1; parts <= 2; ++parts) {
+            for (int ring = kWarps; ring <= max_ring(M); ++ring) {
+                const size_t smem = matvec_smem(M, F, static_cast<int>(P), S, ring, parts);
+                if (smem > kSmemOptIn) break;                 // deeper rings only grow
+                // the exact ring (the whole slice, hv x a multiple of P: no
+                // refills) or a multiple of 8
+                if (ring % kWarps != 0 && ring % (hv * P) != 0) continue;
+                const int64_t cm = matvec_max_clusters(M, F, S, smem);
+                if (cm < 1) continue;
+                const int64_t clusters = std::min<int64_t>(groups, cm);
+                const int64_t tiles = ceil_div(groups, clusters);
+                if ((tiles > 1 ? 2 : 1) != parts) continue;
+                const int64_t recs = tiles * P;               // records of a CTA
+                const int64_t exact = hv * std::max<int64_t>(kWarps / hv, recs);
+                if (ring > exact) break;
+                if (ring != exact && ring % kWarps != 0) continue;
+                const int64_t ctas = clusters * S;
+                const int per_sm = static_cast<int>(ceil_div(ctas, sm_count));
+                const bool two_fit = smem <= half;
+                const double issue = per_sm * static_cast<double>(recs) * rec_t / (per_sm >= 2 ? 1.512 : 1.0);
+                double eff = 1.0;
+                if (ring != exact)
+                    eff = std::min(1.0, std::max(0.05, per_sm * ring * static_cast<double>(slot_bytes(M, F)) /
+                                                           (sm_bw * 2.24)));
+                const double loop = std::max(issue, hbm_t / eff);
+                const int64_t tasks = M <= 4 ? 2 * P * M : 2 * P;
+                const int64_t per_round = M <= 4 ? 8 * 32 : 8 * (64 / M);
+                const double stage = 0.3 * static_cast<double>(ceil_div(tasks, per_round));
+                const double slices = S > 1 ? 0.15 * (S - 2) : 0.0;
+                const double hand = tiles > 1 ? 0.565 * static_cast<double>(tiles * S) : 0.0;
+                // (a second CTA of this call on a few SMs delays only those)
+                const double two_share = std::min(1.0, 4.0 * std::max<double>(0.0, ctas - sm_count) / sm_count);
+                const double no_overlap = 1.476 * (two_fit ? two_share : 1.0);
+                const double cost = 3.0 + stage + loop + slices + hand + no_overlap;
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    best.M = M;
+                    best.fmt = fmt;
+                    best.S = S;
+                    best.clusters = static_cast<int>(clusters);
+                    best.ctas = static_cast<int>(ctas);
+                    best.ring = ring;
+                    best.smem = smem;
+                }
             }
         }
     }
@@ -1226,9 +1362,12 @@ bool plan_matvec_experts(int64_t m, int64_t k, int64_t n, int experts, int sm_co
         for (int two = 1; two >= 0; --two) {
             const size_t limit = two ? half : kSmemOptIn;
             int ring = 0;
-            const int exact = static_cast<int>(std::min<int64_t>(kMaxRing, std::max<int64_t>(kWarps, P)));
-            if (P <= kMaxRing && matvec_smem(M, kFmtQ4, static_cast<int>(P), S, exact, 1) <= limit) ring = exact;
-            for (int64_t r = std::min<int64_t>(kMaxRing, P / kWarps * kWarps); r >= kWarps && ring == 0; r -= kWarps)
+            const int hv = halves(M);
+            const int exact = hv * static_cast<int>(std::max<int64_t>(kWarps / hv, P));
+            if (P * hv <= max_ring(M) && matvec_smem(M, kFmtQ4, static_cast<int>(P), S, exact, 1) <= limit)
+                ring = exact;
+            for (int64_t r = std::min<int64_t>(max_ring(M), P * hv / kWarps * kWarps); r >= kWarps && ring == 0;
+                 r -= kWarps)
                 if (matvec_smem(M, kFmtQ4, static_cast<int>(P), S, static_cast<int>(r), 1) <= limit)
                     ring = static_cast<int>(r);
             if (ring == 0) continue;
@@ -1238,7 +1377,7 @@ bool plan_matvec_experts(int64_t m, int64_t k, int64_t n, int experts, int sm_co
             const int64_t clusters = groups * experts;
             const double waves = static_cast<double>(ceil_div(clusters, cmax));
             const double cost = waves * (static_cast<double>(P) + 4.0) + (S > 1 ? 2.0 : 0.0) +
-                                (P > ring ? static_cast<double>(P - ring) : 0.0);
+                                (P * hv > ring ? static_cast<double>(P - ring / hv) : 0.0);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.M = M;
