@@ -70,11 +70,38 @@ SWEEP = [
     dict(name="W4A8 decode up-projection", m=1, n=9728, k=2560, w4a8=True),
     dict(name="W4A8 slot sweep 14336x4096", m=8, n=14336, k=4096, w4a8=True),
     dict(name="W4A8 slot sweep 14336x4096", m=16, n=14336, k=4096, w4a8=True),
+    # per-output-channel int8 weights (q4_w8_matmul): n x k int8 codes plus
+    # n fp32 scales per call
+    dict(name="int8-weight decode up-projection", m=1, n=9728, k=2560, w8=True),
+    dict(name="int8-weight 4 slots, up-projection", m=4, n=9728, k=2560, w8=True),
+    dict(name="int8-weight slot sweep 14336x4096", m=16, n=14336, k=4096, w8=True),
+    # a mixture layer (q4_0_matmul_experts): 8 experts of 9728 x 2560 with
+    # 1..16 token rows each, one launch; weight bytes of all 8 experts
+    dict(name="8 experts x 9728x2560, mixed group sizes", m=40, n=9728, k=2560,
+         experts=[1, 3, 2, 5, 1, 4, 8, 16]),
 ]
+
+# Token rows at which one expert's layer is better served by the tensor-core
+# GEMM than by the mat-vec (in calls of at most 16 rows): both timed at each m.
+CROSSOVER = dict(n=9728, k=2560, ms=[8, 16, 17, 24, 32, 48, 64, 96])
 
 
 def weight_bytes(n, k):
     return n * (k // 32) * 18
+
+
+def w8_weight_bytes(n, k):
+    """Bytes a call on per-output-channel int8 weights reads: codes and scales."""
+    return n * k + 4 * n
+
+
+def sweep_weight_bytes(cfg):
+    n, k = cfg["n"], cfg["k"]
+    if cfg.get("w8"):
+        return w8_weight_bytes(n, k)
+    if cfg.get("experts"):
+        return len(cfg["experts"]) * weight_bytes(n, k)
+    return weight_bytes(n, k)
 
 
 def decode_kernel_name(m, n=0, sm_count=152):
@@ -205,31 +232,60 @@ class ClockSampler:
 class Workload:
     """Packed weight copies, X and Y resident on the GPU for one shape."""
 
-    def __init__(self, q4lib, m, n, k, min_copies=1, w4a8=False):
+    def __init__(self, q4lib, m, n, k, min_copies=1, w4a8=False, w8=False, experts=None, chunk=0):
+        """w4a8: the integer-dot call; w8: per-output-channel int8 weights
+        (fp32 N(0, 1) * 0.02 weights quantised on the GPU); experts: token
+        rows per expert (one weight set per expert, rows in expert order);
+        chunk: run the m rows as calls of at most `chunk` rows."""
         import torch
         from q4_quantized_linear_gb300 import synth
         self.m, self.n, self.k = m, n, k
-        self.w4a8 = w4a8
+        self.w4a8, self.w8, self.chunk = w4a8, w8, chunk
+        self.experts = list(experts) if experts else None
         self.blocks = synth.q4_0_blocks(n, k, seed=0)
         self.X = synth.activations(m, k, seed=0)
-        wb = weight_bytes(n, k)
+        per_set = len(self.experts) if self.experts else 1
+        wb = (w8_weight_bytes(n, k) if w8 else weight_bytes(n, k)) * per_set
         self.copies = max(min_copies, -(-2 * L2_BYTES // wb) + 1)
-        dev_blocks = torch.from_numpy(self.blocks.reshape(-1)).cuda()
-        base = torch.empty(q4lib.q4_0_packed_size(n, k), dtype=torch.uint8, device="cuda")
-        q4lib.q4_0_pack(base, dev_blocks, n, k)
-        self.W = [base] + [base.clone() for _ in range(self.copies - 1)]
-        del dev_blocks
+        if w8:
+            Wf = torch.from_numpy(synth.activations(n, k, seed=5)).cuda() * 0.02
+            base = torch.empty(q4lib.q4_w8_packed_size(n, k), dtype=torch.uint8, device="cuda")
+            q4lib.q4_w8_quantize(base, Wf, n, k)
+            del Wf
+        else:
+            dev_blocks = torch.from_numpy(self.blocks.reshape(-1)).cuda()
+            base = torch.empty(q4lib.q4_0_packed_size(n, k), dtype=torch.uint8, device="cuda")
+            q4lib.q4_0_pack(base, dev_blocks, n, k)
+            del dev_blocks
+        self.W = [base] + [base.clone() for _ in range(self.copies * per_set - 1)]
+        if self.experts:
+            self.offsets = [0]
+            for c in self.experts:
+                self.offsets.append(self.offsets[-1] + c)
+            assert self.offsets[-1] == m
         self.Xd = torch.from_numpy(self.X).cuda()
         self.Yd = torch.empty((m, n), dtype=torch.float32, device="cuda")
         self.ws, self.wsb = q4lib.workspace_for(m, k, n)
         torch.cuda.synchronize()
 
     def step(self, q4lib, i, stream):
-        if self.w4a8:
-            q4lib.q4_0_matmul_w4a8(self.W[i % self.copies], self.Xd, self.Yd, self.m, self.k, self.n, stream)
-            return
-        q4lib.q4_0_matmul_ws(self.W[i % self.copies], self.Xd, self.Yd, self.m, self.k, self.n,
-                             self.ws, self.wsb, stream)
+        c = i % self.copies
+        if self.experts:
+            E = len(self.experts)
+            q4lib.q4_0_matmul_experts(self.W[c * E:(c + 1) * E], self.offsets, self.Xd, self.Yd, self.k, self.n,
+                                      stream)
+        elif self.w8:
+            q4lib.q4_w8_matmul(self.W[c], self.Xd, self.Yd, self.m, self.k, self.n, stream)
+        elif self.w4a8:
+            q4lib.q4_0_matmul_w4a8(self.W[c], self.Xd, self.Yd, self.m, self.k, self.n, stream)
+        elif self.chunk:
+            for r0 in range(0, self.m, self.chunk):
+                r = min(self.chunk, self.m - r0)
+                q4lib.q4_0_matmul_ws(self.W[c], self.Xd[r0:], self.Yd[r0:], r, self.k, self.n,
+                                     self.ws, self.wsb, stream)
+        else:
+            q4lib.q4_0_matmul_ws(self.W[c], self.Xd, self.Yd, self.m, self.k, self.n,
+                                 self.ws, self.wsb, stream)
 
 
 def reduce_max(value):
@@ -380,9 +436,11 @@ def run_sweep(q4lib, stream, peaks):
     out = []
     for cfg in SWEEP:
         m, n, k = cfg["m"], cfg["n"], cfg["k"]
-        wl = Workload(q4lib, m, n, k, w4a8=cfg.get("w4a8", False))
-        wb = weight_bytes(n, k)
-        est = wb / (peaks["hbm_gbs"] * 1e9) if m <= 16 else 2.0 * m * n * k / (peaks["bf16_tflops"] * 1e12)
+        wl = Workload(q4lib, m, n, k, w4a8=cfg.get("w4a8", False), w8=cfg.get("w8", False),
+                      experts=cfg.get("experts"))
+        wb = sweep_weight_bytes(cfg)
+        decode = m <= 16 or bool(cfg.get("experts"))
+        est = wb / (peaks["hbm_gbs"] * 1e9) if decode else 2.0 * m * n * k / (peaks["bf16_tflops"] * 1e12)
         steps = int(min(20000, max(200, 0.25 / max(est, 1e-7))))
         steps -= steps % wl.copies
         steps = max(steps, wl.copies)
@@ -393,7 +451,7 @@ def run_sweep(q4lib, stream, peaks):
         if n * k <= 1 << 20:
             # a layer this small is a latency case: one isolated call as well
             rec["single_call_latency_us"] = time_single(q4lib, wl, stream)
-        if m <= 16:
+        if decode:
             rec["frac_hbm"] = rec["weight_gbs"] / peaks["hbm_gbs"]
         else:
             rec["tflops"] = 2.0 * m * n * k / t / 1e12
@@ -401,6 +459,28 @@ def run_sweep(q4lib, stream, peaks):
         out.append(rec)
         del wl
         torch.cuda.empty_cache()
+    return out
+
+
+def run_crossover(q4lib, stream):
+    """One expert's layer at m token rows: the library's own dispatch (the
+    mat-vec up to 16 rows, the tensor-core GEMM above) against the mat-vec
+    in calls of at most 16 rows. Microseconds per layer."""
+    import torch
+    n, k = CROSSOVER["n"], CROSSOVER["k"]
+    out = []
+    for m in CROSSOVER["ms"]:
+        rec = dict(m=m, n=n, k=k)
+        for key, chunk in (("dispatch_us", 0), ("matvec_chunks_us", 16)):
+            if chunk and m <= 16:
+                continue
+            wl = Workload(q4lib, m, n, k, chunk=chunk)
+            steps = 2000 - 2000 % wl.copies
+            sec, _ = time_graph(q4lib, wl, steps, 20, stream)
+            rec[key] = sec / steps * 1e6
+            del wl
+            torch.cuda.empty_cache()
+        out.append(rec)
     return out
 
 
@@ -503,6 +583,7 @@ def native(args):
 
     gpu_Y = wl.Yd.cpu().numpy()
     sweep = run_sweep(q4lib, stream, peaks) if (rank == 0 and not args.no_sweep) else None
+    crossover = run_crossover(q4lib, stream) if (rank == 0 and not args.no_sweep) else None
     if world > 1:
         dist.barrier()
     if rank != 0:
@@ -563,6 +644,8 @@ def native(args):
         line["cpu_baseline"] = cpu
     if sweep is not None:
         line["sweep"] = sweep
+    if crossover is not None:
+        line["expert_crossover"] = crossover
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -68,6 +68,8 @@ typedef struct CUstream_st *q4mm_stream_t;
 #define Q4_ERR_NO_MEMORY 7          /* the library could not allocate its own workspace */
 #define Q4_ERR_IO 8                 /* a file could not be opened or read */
 #define Q4_ERR_FORMAT 9             /* a file breaks the GGUF layout (q4_gguf_open) */
+#define Q4_ERR_DEVICE_CHECK 10      /* checked build: a kernel found an index or offset out of range and
+                                       skipped the access (read by q4_last_device_status) */
 
 /*
  * Packed weight layout (what q4_0_pack writes). Repacking the blocks at load
@@ -154,10 +156,13 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
  * Y[r] = X[r] . W_e^T for those rows (golem-server, "Several conversations,
  * in one pass", on mixture layers: the weights an expert contributes are read
  * once for the columns routed to it). Each expert's weights are read once for
- * its rows: the experts with 1..16 rows share one launch of the decode
- * mat-vec per set of up to 32 of them (a thread-block cluster per 128-row
- * group of an expert), larger groups run the tensor-core GEMM one expert at a
- * time; each group has q4_0_matmul's precision for its size.
+ * its rows (twice for 17..24 rows): experts with up to 24 rows run the decode
+ * mat-vec in pieces of at most 16 rows, pieces of the same mat-vec instance
+ * (1, 2, 4, 8 or 16 token columns) sharing one launch per set of up to 32 (a
+ * thread-block cluster per 128-row group of a piece); larger groups run the
+ * tensor-core GEMM one expert at a time (the switch at 24 rows is measured on
+ * GB300: below it the pieces are faster than the GEMM). Each piece or group
+ * has q4_0_matmul's precision for its size.
  *   W_packed: host array of n_experts device pointers, each packed by
  *   q4_0_pack for (n, k), 16-byte aligned (an expert with no rows may be
  *   NULL).
@@ -168,7 +173,7 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
  * The arguments are checked before anything is launched; if a later group
  * is refused (its plan, or the library workspace while a stream is being
  * captured), the groups before it have been written. Scratch: as
- * q4_0_matmul (the library's workspace, for groups of more than 16 rows). */
+ * q4_0_matmul (the library's workspace, for groups of more than 24 rows). */
 Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t n_experts, const int64_t *offsets,
                                  const float *X, float *Y, int64_t k, int64_t n, q4mm_stream_t stream);
 
@@ -283,13 +288,29 @@ Q4MM_API int q4_0_matmul_batched_slots_ws(const void *W_packed, const float *X_s
 /* Human-readable name of a status code (static string, never NULL). */
 Q4MM_API const char *q4_status_string(int status);
 
-/* Device status word of the current device: Q4_OK, or Q4_ERR_DEVICE_TIMEOUT
- * if a kernel's bounded wait ran out since the word was last cleared.
- * Synchronises the device. clear != 0 resets the word to Q4_OK. */
+/* Device status word of the current device: Q4_OK, Q4_ERR_DEVICE_TIMEOUT if
+ * a kernel's bounded wait ran out, or Q4_ERR_DEVICE_CHECK (checked build
+ * only) if a kernel's range check failed, since the word was last cleared
+ * (the first such event is kept). Synchronises the device. clear != 0 resets
+ * the word to Q4_OK. */
 Q4MM_API int q4_last_device_status(int clear);
 
+/* How this library was built: bit 0 set for the checked build (-DQ4MM_CHECKED:
+ * the decode mat-vec checks its shared-memory layout against the launch's
+ * size, every weight record it copies against the layer's records and
+ * every slot row against the ring, and on a failed check records
+ * Q4_ERR_DEVICE_CHECK in the status word and skips the access instead of
+ * faulting), bit 1 for the event-trace build (-DQ4MM_TRACE). */
+Q4MM_API int q4_build_flags(void);
+
 /* Limit, in nanoseconds, on each device-side wait of the library's kernels
- * (default 2e9). Applies to launches made after the call, on every device. */
+ * (default 2e9). Applies to launches made after the call, on every device.
+ * A wait that runs out sets Q4_ERR_DEVICE_TIMEOUT in the device status word
+ * and the kernel returns without its result. The decode mat-vec (the default
+ * path for m <= 16) then still waits, for at least 0.2 s, for the transfers
+ * already issued into its own shared memory, so any limit >= 1 is safe there;
+ * the other kernels take the limit as given for every wait and need one well
+ * above their transfers' latency (>= 1 ms). */
 Q4MM_API int q4_set_wait_limit_ns(uint64_t ns);
 
 /* Declare packed weights read-only while matmuls run (default: not declared).

@@ -49,6 +49,7 @@ _SIGS = {
     "q4_0_matmul_batched_slots_ws": (_INT, [_P, _P, _I64, _P, _I64, _P, _I64, _I64, _I64, _P, _SZ, _P]),
     "q4_status_string": (ctypes.c_char_p, [_INT]),
     "q4_last_device_status": (_INT, [_INT]),
+    "q4_build_flags": (_INT, []),
     "q4_set_wait_limit_ns": (_INT, [ctypes.c_uint64]),
     "q4_set_weight_prefetch": (_INT, [_INT]),
     "q4_set_decode_kernel": (_INT, [_INT]),
@@ -80,6 +81,7 @@ Q4_ERR_WORKSPACE = 6
 Q4_ERR_NO_MEMORY = 7
 Q4_ERR_IO = 8
 Q4_ERR_FORMAT = 9
+Q4_ERR_DEVICE_CHECK = 10
 GGUF_TYPE_Q4_0 = 2
 
 
@@ -219,6 +221,11 @@ def q4_0_matmul_batched_slots_ws(W_packed, X_slots, ldx: int, slot_ids, m: int, 
 
 def q4_last_device_status(clear: bool = True) -> int:
     return int(_lib.q4_last_device_status(1 if clear else 0))
+
+
+def q4_build_flags() -> int:
+    """Bit 0: the checked build (-DQ4MM_CHECKED); bit 1: the trace build."""
+    return int(_lib.q4_build_flags())
 
 
 def q4_set_wait_limit_ns(ns: int) -> int:

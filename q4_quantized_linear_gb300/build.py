@@ -19,6 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libq4mm.so")
 TRACE_BUILD = os.path.join(PKG, "_build_trace")
 TRACE_LIB = os.path.join(TRACE_BUILD, "libq4mm.so")
+CHECKED_BUILD = os.path.join(PKG, "_build_checked")
+CHECKED_LIB = os.path.join(CHECKED_BUILD, "libq4mm.so")
 HEADER = os.path.join(ROOT, "include", "q4mm.h")
 
 SOURCES = ["q4mm_api.cu", "q4mm_pack.cu", "q4mm_decode.cu", "q4mm_gemv.cu", "q4mm_mmv.cu", "q4mm_matvec.cu", "q4mm_w8.cu", "q4mm_prefill.cu",
@@ -60,11 +62,17 @@ def _compile(src: str, verbose_ptxas: bool, outdir: str = BUILD, extra: tuple = 
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False) -> str:
+def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False, checked: bool = False) -> str:
     """Compile libq4mm. trace=True makes the profiling build (in-kernel event
-    trace, -DQ4MM_TRACE) in a separate directory."""
-    outdir, lib = (TRACE_BUILD, TRACE_LIB) if trace else (BUILD, LIB)
-    extra = ("-DQ4MM_TRACE",) if trace else ()
+    trace, -DQ4MM_TRACE), checked=True the debug build whose decode kernel
+    checks its indices and offsets and reports a failed check in the status
+    word (-DQ4MM_CHECKED); each in a directory of its own."""
+    if trace:
+        outdir, lib, extra = TRACE_BUILD, TRACE_LIB, ("-DQ4MM_TRACE",)
+    elif checked:
+        outdir, lib, extra = CHECKED_BUILD, CHECKED_LIB, ("-DQ4MM_CHECKED",)
+    else:
+        outdir, lib, extra = BUILD, LIB, ()
     os.makedirs(outdir, exist_ok=True)
     if force:
         for f in os.listdir(outdir):
@@ -87,4 +95,5 @@ def build(force: bool = False, verbose_ptxas: bool = False, trace: bool = False)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv,
+                checked="--checked" in sys.argv))

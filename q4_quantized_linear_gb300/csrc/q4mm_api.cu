@@ -523,8 +523,21 @@ Q4MM_API const char *q4_status_string(int status)
     case Q4_ERR_NO_MEMORY: return "out of device memory";
     case Q4_ERR_IO: return "file could not be opened or read";
     case Q4_ERR_FORMAT: return "file breaks the GGUF layout";
+    case Q4_ERR_DEVICE_CHECK: return "a kernel's range check failed (checked build)";
     default: return "unknown status";
     }
+}
+
+Q4MM_API int q4_build_flags(void)
+{
+    int f = 0;
+#ifdef Q4MM_CHECKED
+    f |= 1;
+#endif
+#ifdef Q4MM_TRACE
+    f |= 2;
+#endif
+    return f;
 }
 
 Q4MM_API int q4_last_device_status(int clear)

@@ -86,6 +86,21 @@ __device__ __forceinline__ void record_status(int *status, int code)
     if (status) atomicCAS(status, 0, code);
 }
 
+// Range check of the checked build (-DQ4MM_CHECKED): true when `ok`; else
+// records Q4_ERR_DEVICE_CHECK (10) and returns false, so that the caller
+// skips the access. Always true in the ordinary build.
+__device__ __forceinline__ bool q4_check(bool ok, int *status)
+{
+#ifdef Q4MM_CHECKED
+    if (!ok) record_status(status, 10);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    return true;
+#endif
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
@@ -153,8 +168,45 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 // completes (measured on GB300: ~170 ns after a local arrival, ~450 ns after
 // a remote one; a try_wait given a suspend-time hint resumed ~560 ns after a
 // local arrival, so none is given).
+// Non-blocking test of a phase (this CTA's barrier, or acquire at cluster scope).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Below this limit a wait polls without suspending (try_wait may sleep for
+// longer than the limit inside one call), so that the limit is honoured.
+constexpr uint64_t kShortWaitNs = 100000;
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
+    if (limit_ns < kShortWaitNs) {
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -165,6 +217,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
+    if (limit_ns < kShortWaitNs) {
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            if (mbar_test_wait_cluster(bar, parity)) return true;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {

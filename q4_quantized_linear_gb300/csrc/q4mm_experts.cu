@@ -6,9 +6,15 @@
 // pass, for the columns routed to them, with the page's measured switch from
 // per-column to per-expert work at about thirty-two columns. Here X's rows
 // come grouped by expert (offsets[e] .. offsets[e+1] - 1 for expert e) and
-// each expert's weights are read once for its rows: the experts with up to
-// 16 rows share one launch of the decode mat-vec (a cluster per group of an
-// expert's rows), larger groups run the tensor-core GEMM.
+// each expert's weights are read once for its rows (twice for 17..24 rows):
+//   up to 24 rows: the decode mat-vec, in pieces of at most 16 rows; pieces
+//     of the same mat-vec instance (1, 2, 4, 8 or 16 token columns) share one
+//     launch, a cluster per 128-row group of an expert's piece;
+//   more rows: the tensor-core GEMM, one call per expert.
+// The switch at 24 rows is measured on GB300 for a 9728 x 2560 expert: the
+// mat-vec in pieces of 16 rows is faster up to 24 rows (19.0 us at 17 rows
+// against 22.5 us for the GEMM), the GEMM from 32 rows on (22.6 us against
+// 24.0 us).
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -40,40 +46,46 @@ extern "C" Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t
     }
     if (!aligned_to(X, 16) || !aligned_to(Y, 4)) return Q4_ERR_ALIGNMENT;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Experts with 1..16 rows: one launch of the mat-vec per set of up to 32
-    // of them, every expert's weights read once for its rows. Larger groups:
-    // q4_0_matmul each (the tensor-core GEMM).
-    q4::ExpertSet set;
-    int max_m = 0;
-    auto flush = [&]() -> int {
-        if (set.count == 0) return Q4_OK;
-        int rc = q4::launch_expert_set(set, max_m, X, Y, k, n, s);
-        if (rc == Q4_ERR_INVALID_ARG)   // no plan for this shape: one by one
-            for (int i = 0; i < set.count && (rc == Q4_ERR_INVALID_ARG || rc == Q4_OK); ++i)
-                rc = q4_0_matmul(set.W[i], X + static_cast<int64_t>(set.row0[i]) * k,
-                                 Y + static_cast<int64_t>(set.row0[i]) * n, set.m[i], k, n, stream);
-        set.count = 0;
-        max_m = 0;
-        return rc;
-    };
-    for (int64_t e = 0; e < n_experts; ++e) {
-        const int64_t r0 = offsets[e], m = offsets[e + 1] - offsets[e];
-        if (m == 0 || m > 16) continue;
-        set.row0[set.count] = static_cast<int>(r0);
-        set.m[set.count] = static_cast<int>(m);
-        set.W[set.count] = static_cast<const uint8_t *>(W_packed[e]);
-        ++set.count;
-        max_m = std::max(max_m, static_cast<int>(m));
-        if (set.count == q4::kMaxExpertSet) {
-            const int rc = flush();
-            if (rc != Q4_OK) return rc;
+    // Pieces of up to 16 rows of the experts with up to kMatvecRows rows, set
+    // by set: one launch of the mat-vec per instance and per 32 pieces.
+    constexpr int64_t kMatvecRows = 24;
+    constexpr int kInstances[5] = {1, 2, 4, 8, 16};
+    int rc = Q4_OK;
+    for (int inst = 0; inst < 5 && rc == Q4_OK; ++inst) {
+        const int lo = inst == 0 ? 1 : kInstances[inst - 1] + 1, hi = kInstances[inst];
+        q4::ExpertSet set;
+        int max_m = 0;
+        auto flush = [&]() -> int {
+            if (set.count == 0) return Q4_OK;
+            int r = q4::launch_expert_set(set, max_m, X, Y, k, n, s);
+            if (r == Q4_ERR_INVALID_ARG)   // no plan for this shape: piece by piece
+                for (int i = 0; i < set.count && (r == Q4_ERR_INVALID_ARG || r == Q4_OK); ++i)
+                    r = q4_0_matmul(set.W[i], X + static_cast<int64_t>(set.row0[i]) * k,
+                                    Y + static_cast<int64_t>(set.row0[i]) * n, set.m[i], k, n, stream);
+            set.count = 0;
+            max_m = 0;
+            return r;
+        };
+        for (int64_t e = 0; e < n_experts && rc == Q4_OK; ++e) {
+            const int64_t m = offsets[e + 1] - offsets[e];
+            if (m == 0 || m > kMatvecRows) continue;
+            for (int64_t r0 = offsets[e]; r0 < offsets[e + 1] && rc == Q4_OK; r0 += 16) {
+                const int pm = static_cast<int>(std::min<int64_t>(16, offsets[e + 1] - r0));
+                if (pm < lo || pm > hi) continue;
+                set.row0[set.count] = static_cast<int>(r0);
+                set.m[set.count] = pm;
+                set.W[set.count] = static_cast<const uint8_t *>(W_packed[e]);
+                ++set.count;
+                max_m = std::max(max_m, pm);
+                if (set.count == q4::kMaxExpertSet) rc = flush();
+            }
         }
+        if (rc == Q4_OK) rc = flush();
     }
-    int rc = flush();
     if (rc != Q4_OK) return rc;
     for (int64_t e = 0; e < n_experts; ++e) {
         const int64_t r0 = offsets[e], m = offsets[e + 1] - offsets[e];
-        if (m <= 16) continue;
+        if (m <= kMatvecRows) continue;
         // row r0 of X starts on a 16-byte boundary: k is a multiple of 32
         rc = q4_0_matmul(W_packed[e], X + r0 * k, Y + r0 * n, m, k, n, stream);
         if (rc != Q4_OK) return rc;

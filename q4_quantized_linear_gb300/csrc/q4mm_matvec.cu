@@ -84,6 +84,11 @@ namespace q4 {
 namespace {
 
 constexpr int kErrTimeout = 5;                   // Q4_ERR_DEVICE_TIMEOUT
+// After a wait gave up, the waits for what is still landing in this CTA's
+// shared memory (its bulk copies, the other slices' stores) are bounded by
+// at least this, whatever the caller's limit: those transfers are already
+// issued and end in microseconds, and the CTA must not exit before them.
+constexpr uint64_t kDrainNs = 200000000ull;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSliceRows = kGroupRows / kWarps;  // rows of a group each warp finishes
@@ -221,6 +226,18 @@ __device__ __forceinline__ void mma_acc_f16(float (&d)[4], const uint32_t (&a)[4
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A * B + C, m16n8k16, fp16 operands, fp32 accumulate, C left as it is
+// (a start shared by many tiles).
+__device__ __forceinline__ void mma_f16_c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                          const float (&c)[4])
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+                   "f"(c[3]));
+}
+
 // D = A * B, m16n8k16, fp16 operands, fp32 result from a zero start.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
@@ -333,6 +350,7 @@ __device__ __forceinline__ void stage_x(const DecodeArgs &a, const VSmem &sm, in
             xb[i] = xa[i];
             if (e < E && blk < a.nb && tok < a.m) {
                 const int xrow = a.rows ? __ldg(a.rows + tok) : tok;
+                if (!q4_check(xrow >= 0, a.status)) continue;
                 const float *xr = a.X + static_cast<int64_t>(xrow) * a.ldx + 32 * blk + 4 * t;
                 xa[i] = __ldg(reinterpret_cast<const float4 *>(xr));
                 xb[i] = __ldg(reinterpret_cast<const float4 *>(xr + 16));
@@ -438,6 +456,7 @@ __device__ __forceinline__ void stage_x_wide(const DecodeArgs &a, const VSmem &s
     for (int h = 0; h < H; ++h) {
         const int tok = 8 * h + j;
         xrow[h] = tok < a.m ? (a.rows ? __ldg(a.rows + tok) : tok) : -1;
+        if (tok < a.m && !q4_check(xrow[h] >= 0, a.status)) xrow[h] = -1;
     }
     for (int e0 = w; e0 < E; e0 += kWarps * kBatch) {
         float4 xa[kBatch][H], xb[kBatch][H];
@@ -524,6 +543,7 @@ __device__ __forceinline__ void stage_x_w8(const DecodeArgs &a, const VSmem &sm,
             // blocks: its lanes t = 2, 3 read zeros)
             if (e < E && col < 32 * a.nb && tok < a.m) {
                 const int xrow = a.rows ? __ldg(a.rows + tok) : tok;
+                if (!q4_check(xrow >= 0, a.status)) continue;
                 const float *xr = a.X + static_cast<int64_t>(xrow) * a.ldx + col;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) xv[i][j] = __ldg(reinterpret_cast<const float4 *>(xr + 4 * j));
@@ -612,6 +632,7 @@ __device__ __forceinline__ void record_mma(const VSmem &sm, uint32_t rec, int p,
         const float4 cr = ld128f(smem_u32(sm.xp + (p * 2 + bt) * M + (M == 1 ? 0 : (t & 1))));
         const float su = cr.z;
         const int sh = 16 * bt;                     // the block's half of a scale word
+        const float cq[4] = {EXACT ? 0.f : cr.x, EXACT ? 0.f : cr.y, EXACT ? 0.f : cr.x, EXACT ? 0.f : cr.y};
         static_for<8>([&](auto RT) {
             constexpr int rt = decltype(RT)::value;
             const uint32_t w00 = ld32o<kRecQs0Off + 256 * rt>(bq), w01 = ld32o<kRecQs0Off + 256 * rt + 128>(bq);
@@ -624,8 +645,8 @@ __device__ __forceinline__ void record_mma(const VSmem &sm, uint32_t rec, int p,
             weights_f16<EXACT>(w11, a[1][0][1], a[1][0][3], a[1][1][1], a[1][1][3]);
             // both k-steps of both blocks into one tile, from the columns'
             // corrections
-            float D[4] = {EXACT ? 0.f : cr.x, EXACT ? 0.f : cr.y, EXACT ? 0.f : cr.x, EXACT ? 0.f : cr.y};
-            mma_acc_f16(D, a[0][0], B0.x, B0.y);
+            float D[4];
+            mma_f16_c(D, a[0][0], B0.x, B0.y, cq);
             mma_acc_f16(D, a[1][0], B1.x, B1.y);
             mma_acc_f16(D, a[0][1], B0.z, B0.w);
             mma_acc_f16(D, a[1][1], B1.z, B1.w);
@@ -640,6 +661,8 @@ __device__ __forceinline__ void record_mma(const VSmem &sm, uint32_t rec, int p,
         const float4 c0 = ld128f(smem_u32(sm.xp + p * 2 * 4 + t));
         const float4 c1 = ld128f(smem_u32(sm.xp + (p * 2 + 1) * 4 + t));
         const float su0 = c0.z, su1 = c1.z;
+        const float cq0[4] = {EXACT ? 0.f : c0.x, EXACT ? 0.f : c0.y, EXACT ? 0.f : c0.x, EXACT ? 0.f : c0.y};
+        const float cq1[4] = {EXACT ? 0.f : c1.x, EXACT ? 0.f : c1.y, EXACT ? 0.f : c1.x, EXACT ? 0.f : c1.y};
         static_for<8>([&](auto RT) {
             constexpr int rt = decltype(RT)::value;
             const uint32_t w00 = ld32o<kRecQs0Off + 256 * rt>(bq), w01 = ld32o<kRecQs0Off + 256 * rt + 128>(bq);
@@ -650,10 +673,9 @@ __device__ __forceinline__ void record_mma(const VSmem &sm, uint32_t rec, int p,
             weights_f16<EXACT>(w01, a[0][0][1], a[0][0][3], a[0][1][1], a[0][1][3]);
             weights_f16<EXACT>(w10, a[1][0][0], a[1][0][2], a[1][1][0], a[1][1][2]);
             weights_f16<EXACT>(w11, a[1][0][1], a[1][0][3], a[1][1][1], a[1][1][3]);
-            float D0[4] = {EXACT ? 0.f : c0.x, EXACT ? 0.f : c0.y, EXACT ? 0.f : c0.x, EXACT ? 0.f : c0.y};
-            float D1[4] = {EXACT ? 0.f : c1.x, EXACT ? 0.f : c1.y, EXACT ? 0.f : c1.x, EXACT ? 0.f : c1.y};
-            mma_acc_f16(D0, a[0][0], B0.x, B0.y);
-            mma_acc_f16(D1, a[1][0], B1.x, B1.y);
+            float D0[4], D1[4];
+            mma_f16_c(D0, a[0][0], B0.x, B0.y, cq0);
+            mma_f16_c(D1, a[1][0], B1.x, B1.y, cq1);
             mma_acc_f16(D0, a[0][1], B0.z, B0.w);
             mma_acc_f16(D1, a[1][1], B1.z, B1.w);
             y[rt][0][0] = fmaf(half_of(s0, 0) * su0, fmaf(D0[1], 0x1p-8f, D0[0]), y[rt][0][0]);
@@ -881,7 +903,7 @@ __device__ __forceinline__ void write_rows(const DecodeArgs &a, const VSmem &sm,
             for (int r = 1; r < S; ++r) v += sm.red[((rb * (S - 1) + r - 1) * M + tok) * kGroupRows + row];
             if (a.row_scale) v *= __ldg(a.row_scale + grow);   // int8 weights: the channel's scale
             const int yr = a.rows ? __ldg(a.rows + tok) : tok;
-            a.Y[static_cast<int64_t>(yr) * a.ldy + grow] = v;
+            if (q4_check(yr >= 0, a.status)) a.Y[static_cast<int64_t>(yr) * a.ldy + grow] = v;
         }
     }
 }
@@ -940,6 +962,12 @@ __device__ __forceinline__ void load_item(const DecodeArgs &a, const VSmem &sm, 
                                           int p0, uint64_t pol)
 {
     constexpr int kRB = rec_bytes(F), kSB = slot_bytes(M, F);
+    // (checked build: a record outside the layer or a slot outside the ring
+    // is not copied; a slot's barrier still completes, without data)
+    if (!q4_check(G0 + gi * a.clusters < a.groups && j >= 0 && p0 + j < a.np && s >= 0 && s < a.ring, a.status)) {
+        if (s >= 0 && s < a.ring) mbar_arrive(&sm.full[s]);
+        return;
+    }
     const int64_t rec = static_cast<int64_t>(G0 + gi * a.clusters) * a.np + p0 + j;
     const uint8_t *src = a.W + rec * kRB;
     uint8_t *dst = sm.ring + static_cast<size_t>(s) * kSB;
@@ -1009,7 +1037,7 @@ __device__ __forceinline__ bool consume(const DecodeArgs &a, const VSmem &sm, in
 }
 
 template <int M, int F>
-__global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const DecodeArgs call, const ExpertSet set)
+__global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const DecodeArgs call, const ExpertSet set)
 {
     constexpr int kSB = slot_bytes(M, F);
     constexpr int NS = kWarps / halves(M);
@@ -1069,6 +1097,17 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const DecodeArgs ca
     sm.red_free = sm.red_full + 2 * kWarps;
     sm.red_tx = sm.red_free + 2 * kWarps;
 
+#ifdef Q4MM_CHECKED
+    {
+        // the layout must end inside the launch's dynamic shared memory (the
+        // same for every CTA of the grid: all return together, before any
+        // barrier or copy)
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        const size_t used = static_cast<size_t>(reinterpret_cast<uint8_t *>(sm.red_tx + 1) - smem_raw);
+        if (!q4_check(used <= dyn && R <= max_ring(M) && R >= kWarps / halves(M) * halves(M), a.status)) return;
+    }
+#endif
     if (tid == 0) {
         for (int i = 0; i < R; ++i) mbar_init(&sm.full[i], 1);
         for (int i = 0; i < 2; ++i) {
@@ -1121,8 +1160,9 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const DecodeArgs ca
         // A warp that gave up may still have copies landing in its slots
         // (the records after the last one it read): wait for them, bounded,
         // so that none lands after the CTA has exited.
+        const uint64_t drain_ns = a.wait_ns > kDrainNs ? a.wait_ns : kDrainNs;
         for (int n = pending; n < total && n < pending + sm.rh; n += NS)
-            if (!warp_wait(&sm.full[(c / NS) * sm.rh + n % sm.rh], static_cast<uint32_t>((n / sm.rh) & 1), a.wait_ns))
+            if (!warp_wait(&sm.full[(c / NS) * sm.rh + n % sm.rh], static_cast<uint32_t>((n / sm.rh) & 1), drain_ns))
                 break;
     }
 
@@ -1154,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const DecodeArgs ca
             cluster_wait();
             // every other CTA has sent before arriving: after a wait that gave
             // up, let those stores land before this CTA exits
-            if (!got) warp_wait_cluster(sm.red_tx, 0u, a.wait_ns);
+            if (!got) warp_wait_cluster(sm.red_tx, 0u, a.wait_ns > kDrainNs ? a.wait_ns : kDrainNs);
         }
     } else if (S > 1) {
         // Every CTA of the cluster stays until the others are done with its

@@ -36,9 +36,45 @@ def test_library_exports_every_declared_symbol(q4lib):
 
 
 def test_status_strings(q4lib):
-    for code in range(10):
+    for code in range(11):
         assert q4lib.q4_status_string(code) not in ("", "unknown status")
     assert q4lib.q4_status_string(99) == "unknown status"
+
+
+def test_default_build_is_neither_checked_nor_traced(q4lib):
+    assert q4lib.q4_build_flags() == 0
+
+
+def test_int8_weight_packed_size_formula(q4lib):
+    # records of 128 rows x 64 int8 codes (8192 bytes), then 4 bytes of scale
+    # per padded row
+    assert q4lib.q4_w8_packed_size(9728, 2560) == 76 * 40 * 8192 + 76 * 128 * 4
+    assert q4lib.q4_w8_packed_size(130, 96) == 2 * 2 * 8192 + 2 * 128 * 4
+    assert q4lib.q4_w8_packed_size(0, 64) == 0
+    assert q4lib.q4_w8_packed_size(64, 48) == 0
+
+
+@pytest.mark.parametrize("call,args,code", [
+    ("q4_w8_quantize", (0, 0x1000, 64, 64), 1),                       # null packed
+    ("q4_w8_quantize", (0x1000, 0, 64, 64), 1),                       # null W
+    ("q4_w8_quantize", (0x1000, 0x1000, 64, 48), 1),                  # k % 32 != 0
+    ("q4_w8_quantize", (0x1008, 0x1000, 64, 64), 2),                  # packed not 16-byte aligned
+    ("q4_w8_quantize", (0x1000, 0x1004, 64, 64), 2),                  # W not 16-byte aligned
+    ("q4_w8_unpack", (0, 0x1000, 0x1000, 64, 64), 1),                 # null codes
+    ("q4_w8_unpack", (0x1000, 0x1000, 0x1008, 64, 64), 2),            # packed not 16-byte aligned
+    ("q4_w8_unpack", (0x1001, 0x1000, 0x1000, 64, 64), 2),            # codes not 4-byte aligned
+    ("q4_w8_matmul", (0, 0x1000, 0x1000, 1, 64, 64), 1),              # null packed
+    ("q4_w8_matmul", (0x1000, 0x1000, 0x1000, -1, 64, 64), 1),        # m < 0
+    ("q4_w8_matmul", (0x1000, 0x1000, 0x1000, 1, 64, 0), 1),          # n == 0
+    ("q4_w8_matmul", (0x1000, 0x1004, 0x1000, 1, 64, 64), 2),         # X not 16-byte aligned
+    ("q4_w8_matmul", (0x1000, 0x1000, 0x1002, 1, 64, 64), 2),         # Y not 4-byte aligned
+])
+def test_int8_weight_calls_refuse_bad_arguments_before_device_work(q4lib, call, args, code):
+    assert getattr(q4lib, call)(*args, stream=0, check=False) == code
+
+
+def test_int8_weight_matmul_with_no_rows_is_a_no_op(q4lib):
+    assert q4lib.q4_w8_matmul(0x1000, 0x1000, 0x1000, 0, 64, 64, stream=0, check=False) == 0
 
 
 def test_packed_size_formula(q4lib):

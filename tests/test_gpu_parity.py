@@ -315,6 +315,34 @@ def test_bounded_wait_reports_timeout_and_context_survives(q4lib, oracle_mod):
     assert_parity(Y, Yr, B, m, "after timeout")
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 14336, 4096), (4, 2560, 9728), (16, 1000, 2080)])
+def test_matvec_wait_limit_reports_timeout_and_context_survives(q4lib, oracle_mod, m, n, k):
+    """The decode mat-vec's own bounded waits (ring slots, the warps' partial
+    rows, the K slices' exchange) give up at a 1 ns limit: the call reports
+    Q4_ERR_DEVICE_TIMEOUT through the status word instead of hanging, still
+    lets every copy already in flight land, and the next call with the
+    default limit is correct."""
+    blocks = synth.q4_0_blocks(n, k, seed=81)
+    X = synth.activations(m, k, seed=82)
+    W = pack_dev(q4lib, blocks, n, k)
+    q4lib.q4_last_device_status(clear=True)
+    q4lib.q4_set_decode_kernel(q4lib.Q4_DECODE_MATVEC)
+    Xd = to_dev(X)
+    Yd = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    q4lib.q4_set_wait_limit_ns(1)
+    try:
+        q4lib.q4_0_matmul(W, Xd, Yd, m, k, n)
+        status = q4lib.q4_last_device_status(clear=True)
+    finally:
+        q4lib.q4_set_wait_limit_ns(2_000_000_000)
+        q4lib.q4_set_decode_kernel(q4lib.Q4_DECODE_AUTO)
+    assert status == q4lib.Q4_ERR_DEVICE_TIMEOUT
+    Y = run_matmul(q4lib, W, X, n)
+    assert q4lib.q4_last_device_status(clear=True) == 0
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, "after a wait gave up")
+
+
 # -------------------------------------------------------- expert groups ----
 
 def test_expert_groups_match_the_oracle(q4lib, oracle_mod):
@@ -345,11 +373,13 @@ def test_expert_groups_match_the_oracle(q4lib, oracle_mod):
     (200, 1056, [(e * 7) % 17 for e in range(40)]),                         # two sets of <= 32
     (9728, 2560, [1, 3, 0, 16, 5, 2, 8, 4]),                                # the layer's size
     (96, 2080, [20, 1, 33, 2]),                                             # with GEMM-sized groups
+    (130, 640, [17, 24, 25, 1, 23, 40]),                                    # both sides of the 24-row switch
 ])
 def test_expert_sets_match_the_oracle(q4lib, oracle_mod, n, k, sizes):
-    """Experts of up to 16 rows share one launch of the mat-vec per set of
-    up to 32 (a cluster per group of an expert's rows); each group is checked
-    at its size's tolerance, and rows of other groups are not touched."""
+    """Experts of up to 24 rows run the mat-vec in pieces of at most 16 rows,
+    pieces of one instance sharing a launch per set of up to 32 (a cluster
+    per group of a piece); larger ones the GEMM. Each group is checked at its
+    size's tolerance, and rows of other groups are not touched."""
     offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
     rows = int(offsets[-1])
     experts = [synth.q4_0_blocks(n, k, seed=900 + e) if s_ else None for e, s_ in enumerate(sizes)]
