@@ -53,6 +53,9 @@ WORKLOADS = {
     **{f"sweep-m{m}": dict(name="slot sweep 14336x4096", m=m, n=14336, k=4096) for m in (1, 2, 4, 8, 16)},
     "logit": dict(name="logit head", m=4, n=151936, k=2560),
     "prefill": dict(name="prefill", m=540, n=9728, k=2560),
+    # the variants (for profiles): integer-dot X, per-channel int8 weights
+    "w4a8-decode": dict(name="W4A8 decode up-projection", m=1, n=9728, k=2560, w4a8=True),
+    "w8-decode": dict(name="int8-weight decode up-projection", m=1, n=9728, k=2560, w8=True),
 }
 SWEEP = [
     dict(name="single GEMV", m=1, n=1024, k=1024),
@@ -108,7 +111,9 @@ def decode_kernel_name(m, n=0, sm_count=152):
     """The kernel the library's automatic dispatch runs for m token rows."""
     if m > 16:
         return "gemm_kernel (q4mm_prefill.cu, after xcast_kernel)"
-    return "matvec_kernel (q4mm_matvec.cu, whole records per warp, exact block sums on the warp-level MMA)"
+    if m <= 4:
+        return "matvec_kernel (q4mm_matvec.cu, whole records per warp, exact block sums on the warp-level MMA)"
+    return "matvec_kernel (q4mm_matvec.cu, half records per warp, X as one fp16 term per element)"
 
 
 def load_peaks():
@@ -559,11 +564,11 @@ def native(args):
     peaks = load_peaks()
     cfg = WORKLOADS[args.workload]
     m, n, k = cfg["m"], cfg["n"], cfg["k"]
-    wb = weight_bytes(n, k)
+    wb = sweep_weight_bytes(cfg)
     flops = 2.0 * m * n * k
     tensor = m > 16
     stream = torch.cuda.Stream()
-    wl = Workload(q4lib, m, n, k)
+    wl = Workload(q4lib, m, n, k, w4a8=cfg.get("w4a8", False), w8=cfg.get("w8", False))
 
     sampler = ClockSampler(local) if rank == 0 else None
     barrier = dist.barrier if world > 1 else None
@@ -607,9 +612,10 @@ def native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        # decode: bf16 operands (X split into two bf16 terms per block,
-        # weights exact), fp32 accumulation; prefill: bf16, fp32 accumulation
-        "dtype": "bf16" if tensor else "bf16x2",
+        # the operands the tensor cores take, fp32 accumulation throughout:
+        # prefill bf16; decode m <= 4 fp16 weights (exact) against X as two
+        # fp16 fixed-point terms per block; m >= 8 X as one fp16 term
+        "dtype": "bf16" if tensor else ("f16x2" if m <= 4 else "f16"),
         "data": "synthetic",
         "config": {
             "workload": f"{cfg['name']}: Q4_0 W n={n} x k={k}, m={m}",
@@ -633,6 +639,7 @@ def native(args):
             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json {peak_key})" if peaks["source"] == "measured"
             else "fallback",
             "units": ("algorithmic FLOP = 2*m*n*k per step (cast + GEMM launches)" if tensor
+                      else "algorithmic bytes = n*k + 4n int8 codes and scales per launch" if cfg.get("w8")
                       else "algorithmic bytes = n*k/32*18 Q4_0 weight bytes per launch"),
         },
         "e2e": {"value": e2e_value, "unit": unit, "steps": e2e_steps,
