@@ -418,8 +418,10 @@ def time_e2e(q4lib, wl, steps, stream, per_graph=200):
 
 
 def time_single(q4lib, wl, stream, trials=50):
-    """Latency of one isolated call: the device idle before and after, CUDA
-    events around the launch on its stream; the median over trials."""
+    """Device-side latency of one isolated call: no kernel of the library
+    before or after it, CUDA events around it on its stream, the call
+    queued behind a device-side pause so that the host's launch is not
+    timed; the median over trials."""
     import torch
     out = []
     for i in range(trials + 3):
@@ -427,6 +429,7 @@ def time_single(q4lib, wl, stream, trials=50):
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
+            torch.cuda._sleep(SLEEP_CYCLES)
             start.record(stream)
             wl.step(q4lib, i, stream.cuda_stream)
             end.record(stream)

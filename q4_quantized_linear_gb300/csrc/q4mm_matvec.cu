@@ -1279,6 +1279,8 @@ int matvec_max_clusters(int M, int F, int S, size_t smem)
 // microseconds: fitted to graph-replay timings of this kernel on GB300.
 double record_us(int M) { return M <= 1 ? 0.115 : M == 2 ? 0.13 : M == 4 ? 0.195 : M == 8 ? 0.206 : 0.291; }
 
+bool plan_matvec_search(int M, int F, int fmt, int64_t k, int64_t n, int sm_count, MatvecPlan *plan);
+
 } // namespace
 
 // Choose the cluster size S (K slices per 128-row group), the number of
@@ -1301,6 +1303,38 @@ bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan
     // int8 weights stage all four token columns of a tile (m <= 4 share the
     // four-token instance)
     const int M = F == kFmtW8 ? std::max(4, instance_of(m)) : instance_of(m);
+    // a plan depends on the instance, the shape, the format and the device
+    // (its SM count and cluster occupancy): computed once per such key
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int64_t, int64_t, int, int>, MatvecPlan> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const auto key = std::make_tuple(dev, M, k, n, fmt, sm_count);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            if (it->second.ctas == 0) return false;
+            *plan = it->second;
+            return true;
+        }
+    }
+    MatvecPlan found;
+    const bool ok = plan_matvec_search(M, F, fmt, k, n, sm_count, &found);
+    std::lock_guard<std::mutex> lock(mu);
+    cache.emplace(key, ok ? found : MatvecPlan{});
+    if (!ok) return false;
+    *plan = found;
+    return true;
+}
+
+namespace {
+
+bool plan_matvec_search(int M, int F, int fmt, int64_t k, int64_t n, int sm_count, MatvecPlan *plan)
+{
     const int hv = halves(M);
     const int64_t groups = ceil_div(n, kGroupRows);
     const int64_t np = ceil_div(k, kPairK);
@@ -1363,6 +1397,8 @@ bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan
     *plan = best;
     return true;
 }
+
+} // namespace
 
 cudaError_t launch_matvec(const MatvecPlan &plan, const DecodeArgs &args, cudaStream_t s)
 {
