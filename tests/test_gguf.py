@@ -125,3 +125,43 @@ def test_q4_0_tensor_loads_packs_and_multiplies(q4lib, oracle_mod, tmp_path):
     Y = run_matmul(q4lib, W, X, n)
     Yr, B = oracle_mod.matmul(blocks, X, n, k)
     assert_parity(Y, Yr, B, m, "gguf-loaded weights")
+
+
+def _golden_bytes():
+    import os
+    import re
+    here = os.path.dirname(os.path.abspath(__file__))
+    with open(os.path.join(here, "golden", "gguf_min_q4_0.hex")) as f:
+        txt = f.read()
+    return bytes(int(x, 16) for line in txt.splitlines() for x in re.sub(r"#.*", "", line).split())
+
+
+def test_hand_typed_gguf_golden_is_read_as_the_layout_says(q4lib, oracle_mod, tmp_path):
+    """A file typed byte by byte from the container's layout (not written by
+    the test writer): the reader finds the alignment, the one Q4_0 tensor's
+    name, type, dims (innermost first) and the blob offset (128: 98 bytes of
+    header rounded up to 32), and its 36 bytes; the oracle reads them as the
+    weights the file's comments state."""
+    data = _golden_bytes()
+    assert len(data) == 164
+    path = tmp_path / "golden.gguf"
+    path.write_bytes(data)
+    h = q4lib.q4_gguf_open(str(path))
+    try:
+        assert q4lib.q4_gguf_tensor_count(h) == 1
+        assert q4lib.q4_gguf_get_int(h, "general.alignment") == 32
+        assert q4lib.q4_gguf_find_tensor(h, "w") == 0
+        info = q4lib.q4_gguf_tensor_info(h, 0)
+        assert (info["name"], info["type"], info["dims"]) == ("w", Q4_0, [32, 2])
+        assert (info["file_offset"], info["bytes"]) == (128, 36)
+        out = np.zeros(36, dtype=np.uint8)
+        q4lib.q4_gguf_read_tensor(h, 0, out, out.nbytes)
+    finally:
+        q4lib.q4_gguf_close(h)
+    assert out.tobytes() == data[128:]
+    # W^T through the oracle's product with the identity
+    Y, _ = oracle_mod.matmul(out.reshape(2, 1, 18), np.eye(32, dtype=np.float32), 2, 32)
+    low = [-8, -6, -4, -2, 0, 2, 4, 6] * 2        # elements 0..15: the bytes' low nibbles - 8
+    high = [-7, -5, -3, -1, 1, 3, 5, 7] * 2       # elements 16..31: the high nibbles - 8
+    assert np.array_equal(Y[:, 0], np.array(low + high, dtype=np.float64))
+    assert np.array_equal(Y[:, 1], np.zeros(32))
