@@ -275,6 +275,12 @@ __device__ __forceinline__ void cluster_arrive_relaxed()
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Arrive with release semantics: this CTA's writes so far (its barriers'
+// initialisation) are visible to the cluster once the others have waited.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 
 __device__ __forceinline__ unsigned absmax_bits(const float4 &v)
 {
@@ -1130,7 +1136,11 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
     // The next kernel in the stream may be scheduled now: it waits for this
     // one to complete before it reads anything this one writes.
     pdl_launch_dependents();
-    if (S > 1) cluster_sync(); // every CTA's barriers initialised before any remote access
+    // every CTA's barriers are initialised before any remote access: the
+    // cluster barrier's arrive here, its wait after X is staged (no remote
+    // access comes before that), so that its latency hides behind the
+    // staging
+    if (S > 1) cluster_arrive_release();
 
     // Weights may stream before the preceding kernel has finished only when
     // the caller declared them read-only.
@@ -1145,6 +1155,7 @@ __global__ void __launch_bounds__(kThreads, M >= 16 ? 1 : 2) matvec_kernel(const
     else if constexpr (M >= 8) stage_x_wide<M>(a, sm, p0, P, c, lane);
     else stage_x<M>(a, sm, p0, P, c, lane);
     __syncthreads();
+    if (S > 1) cluster_wait();
 
     int pending = c % NS;                             // the warp's first item not yet read
     SliceRows<M> keep;
