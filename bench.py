@@ -367,54 +367,83 @@ def time_graph(q4lib, wl, steps, warmup, stream, per_graph=1000, sampler=None, b
 
 
 def time_e2e(q4lib, wl, steps, stream, per_graph=200):
-    """Public API with pinned host buffers: every step copies X host -> device,
-    calls the layer and copies Y device -> host, all inside the timed region
-    (captured as CUDA graphs of up to per_graph steps, like the device-side
-    timing)."""
+    """Public API with pinned host buffers: every step copies its X host ->
+    device, calls the layer and copies its Y device -> host, all inside the
+    timed region (captured as CUDA graphs of up to per_graph steps, like the
+    device-side timing). Consecutive steps use two device buffer pairs and
+    overlap: step i's input copy runs on a copy-in stream while step i - 1
+    computes, its output copy on a copy-out stream while step i + 1 computes
+    (events order each buffer's writer after its last reader)."""
     import torch
-    Xh = torch.from_numpy(wl.X).pin_memory()
-    Yh = torch.empty((wl.m, wl.n), dtype=torch.float32).pin_memory()
+    Xh = [torch.from_numpy(wl.X).pin_memory() for _ in range(2)]
+    Yh = [torch.empty((wl.m, wl.n), dtype=torch.float32).pin_memory() for _ in range(2)]
+    Xd = [wl.Xd, wl.Xd.clone()]
+    Yd = [wl.Yd, torch.empty_like(wl.Yd)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    saved = (wl.Xd, wl.Yd)
 
-    def one(i):
-        wl.Xd.copy_(Xh, non_blocking=True)
-        wl.step(q4lib, i, stream.cuda_stream)
-        Yh.copy_(wl.Yd, non_blocking=True)
+    def steps_on(count):
+        ev_in = [torch.cuda.Event() for _ in range(count)]
+        ev_k = [torch.cuda.Event() for _ in range(count)]
+        ev_out = [torch.cuda.Event() for _ in range(count)]
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(count):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_k[i - 2])          # step i - 2's kernel has read Xd[b]
+                Xd[b].copy_(Xh[b], non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])          # step i - 2's Y has left Yd[b]
+            wl.Xd, wl.Yd = Xd[b], Yd[b]
+            wl.step(q4lib, i, stream.cuda_stream)
+            ev_k[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_k[i])
+                Yh[b].copy_(Yd[b], non_blocking=True)
+                ev_out[i].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
 
     per_graph = max(1, min(per_graph, steps))
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            one(i)
-    torch.cuda.synchronize()
-    graphs = {}
+    try:
+        with torch.cuda.stream(stream):
+            steps_on(3)
+        torch.cuda.synchronize()
+        graphs = {}
 
-    def graph(count):
-        if count not in graphs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                with torch.cuda.graph(g, stream=stream):
-                    for i in range(count):
-                        one(i)
-            graphs[count] = g
-        return graphs[count]
+        def graph(count):
+            if count not in graphs:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    with torch.cuda.graph(g, stream=stream):
+                        steps_on(count)
+                graphs[count] = g
+            return graphs[count]
 
-    g_full = graph(per_graph)
-    rest = steps % per_graph
-    g_rest = graph(rest) if rest else None
-    with torch.cuda.stream(stream):
-        g_full.replay()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(SLEEP_CYCLES)
-        start.record(stream)
-        for _ in range(steps // per_graph):
+        g_full = graph(per_graph)
+        rest = steps % per_graph
+        g_rest = graph(rest) if rest else None
+        with torch.cuda.stream(stream):
             g_full.replay()
-        if g_rest is not None:
-            g_rest.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    return start.elapsed_time(end) / 1e3, Xh.numel() * 4, Yh.numel() * 4
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SLEEP_CYCLES)
+            start.record(stream)
+            for _ in range(steps // per_graph):
+                g_full.replay()
+            if g_rest is not None:
+                g_rest.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+    finally:
+        wl.Xd, wl.Yd = saved
+    return start.elapsed_time(end) / 1e3, Xh[0].numel() * 4, Yh[0].numel() * 4
 
 
 def time_single(q4lib, wl, stream, trials=50):
