@@ -1304,7 +1304,8 @@ bool plan_matvec_search(int M, int F, int fmt, int64_t k, int64_t n, int sm_coun
 //   of one call on an SM hide each other's latencies), or the layer's HBM
 //   stream if longer, slowed when a refilled ring keeps too few bytes in
 //   flight per SM; a fixed start; X staging in rounds of loads; the slices'
-//   exchange; per-group handshakes of CTAs with several groups; and the
+//   exchange; per-group handshakes of CTAs with several groups and a K
+//   split; and the
 //   start-up that cannot overlap the preceding call when no SM has room for
 //   the next call's CTA.
 bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan, int fmt)
@@ -1355,7 +1356,11 @@ bool plan_matvec_search(int M, int F, int fmt, int64_t k, int64_t n, int sm_coun
     const double hbm_t = static_cast<double>(groups * np) * rec_bytes(F) / (sm_bw * sm_count);
     MatvecPlan best;
     double best_cost = 1e300;
-    for (int S = 1; S <= kMaxSlices && S <= np; ++S) {
+    // With four or more 128-row groups per SM every SM has whole groups to
+    // work on: no K split (measured on the 151936-row logit head at m = 1, 4,
+    // 8 and 16, where the split plans the model would pick were slower).
+    const int max_slices = groups >= 4 * static_cast<int64_t>(sm_count) ? 1 : kMaxSlices;
+    for (int S = 1; S <= max_slices && S <= np; ++S) {
         const int64_t P = ceil_div(np, S);
         for (int parts = 1; parts <= 2; ++parts) {
             for (int ring = kWarps; ring <= max_ring(M); ++ring) {
@@ -1386,7 +1391,9 @@ bool plan_matvec_search(int M, int F, int fmt, int64_t k, int64_t n, int sm_coun
                 const int64_t per_round = M <= 4 ? 8 * 32 : 8 * (64 / M);
                 const double stage = 0.3 * static_cast<double>(ceil_div(tasks, per_round));
                 const double slices = S > 1 ? 0.15 * (S - 2) : 0.0;
-                const double hand = tiles > 1 ? 0.565 * static_cast<double>(tiles * S) : 0.0;
+                // (the handshake crosses the cluster; without a K split the
+                // group's rows are summed inside the CTA)
+                const double hand = tiles > 1 && S > 1 ? 0.565 * static_cast<double>(tiles * S) : 0.0;
                 // (a second CTA of this call on a few SMs delays only those)
                 const double two_share = std::min(1.0, 4.0 * std::max<double>(0.0, ctas - sm_count) / sm_count);
                 const double no_overlap = 1.476 * (two_fit ? two_share : 1.0);
