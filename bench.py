@@ -44,6 +44,8 @@ sys.path.insert(0, ROOT)
 METRIC = "Q4_0 weight GB/s (% HBM peak) at m=1..16; prefill TFLOP/s (% bf16 peak)"
 L2_BYTES = 129 * 1024 * 1024
 SLEEP_CYCLES = 200_000          # about 0.1 ms of device time before a timed region
+NOMINAL_HBM_GBS = 7900.0        # GB300 spec sheet: HBM3e bandwidth
+NOMINAL_BF16_TFLOPS = 2250.0    # GB300 spec sheet: dense bf16 tensor-core peak
 HEADLINE = dict(name="decode GEMV, FFN up-projection", m=1, n=9728, k=2560)
 WORKLOADS = {
     "decode": HEADLINE,
@@ -490,9 +492,11 @@ def run_sweep(q4lib, stream, peaks):
             rec["single_call_latency_us"] = time_single(q4lib, wl, stream)
         if decode:
             rec["frac_hbm"] = rec["weight_gbs"] / peaks["hbm_gbs"]
+            rec["frac_hbm_nominal"] = rec["weight_gbs"] / NOMINAL_HBM_GBS
         else:
             rec["tflops"] = 2.0 * m * n * k / t / 1e12
             rec["frac_bf16"] = rec["tflops"] / peaks["bf16_tflops"]
+            rec["frac_bf16_nominal"] = rec["tflops"] / NOMINAL_BF16_TFLOPS
         out.append(rec)
         del wl
         torch.cuda.empty_cache()
@@ -670,6 +674,10 @@ def native(args):
             "traffic": traffic,
             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json {peak_key})" if peaks["source"] == "measured"
             else "fallback",
+            # the spec sheet's dense figures, as a second reference beside the
+            # measured denominator above (which the fraction uses)
+            "nominal_peak": NOMINAL_BF16_TFLOPS if tensor else NOMINAL_HBM_GBS,
+            "frac_nominal": achieved / (NOMINAL_BF16_TFLOPS if tensor else NOMINAL_HBM_GBS),
             "units": ("algorithmic FLOP = 2*m*n*k per step (cast + GEMM launches)" if tensor
                       else "algorithmic bytes = n*k + 4n int8 codes and scales per launch" if cfg.get("w8")
                       else "algorithmic bytes = n*k/32*18 Q4_0 weight bytes per launch"),

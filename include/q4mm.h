@@ -156,11 +156,11 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
  * Y[r] = X[r] . W_e^T for those rows (golem-server, "Several conversations,
  * in one pass", on mixture layers: the weights an expert contributes are read
  * once for the columns routed to it). Each expert's weights are read once for
- * its rows (twice for 17..24 rows): experts with up to 24 rows run the decode
+ * its rows (twice for 17..32 rows): experts with up to 32 rows run the decode
  * mat-vec in pieces of at most 16 rows, pieces of the same mat-vec instance
  * (1, 2, 4, 8 or 16 token columns) sharing one launch per set of up to 32 (a
  * thread-block cluster per 128-row group of a piece); larger groups run the
- * tensor-core GEMM one expert at a time (the switch at 24 rows is measured on
+ * tensor-core GEMM one expert at a time (the switch at 32 rows is measured on
  * GB300: below it the pieces are faster than the GEMM). Each piece or group
  * has q4_0_matmul's precision for its size.
  *   W_packed: host array of n_experts device pointers, each packed by
@@ -173,7 +173,7 @@ Q4MM_API int q4_0_matmul_ws(const void *W_packed, const float *X, float *Y,
  * The arguments are checked before anything is launched; if a later group
  * is refused (its plan, or the library workspace while a stream is being
  * captured), the groups before it have been written. Scratch: as
- * q4_0_matmul (the library's workspace, for groups of more than 24 rows). */
+ * q4_0_matmul (the library's workspace, for groups of more than 32 rows). */
 Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t n_experts, const int64_t *offsets,
                                  const float *X, float *Y, int64_t k, int64_t n, q4mm_stream_t stream);
 

@@ -6,15 +6,15 @@
 // pass, for the columns routed to them, with the page's measured switch from
 // per-column to per-expert work at about thirty-two columns. Here X's rows
 // come grouped by expert (offsets[e] .. offsets[e+1] - 1 for expert e) and
-// each expert's weights are read once for its rows (twice for 17..24 rows):
-//   up to 24 rows: the decode mat-vec, in pieces of at most 16 rows; pieces
+// each expert's weights are read once for its rows (twice for 17..32 rows):
+//   up to 32 rows: the decode mat-vec, in pieces of at most 16 rows; pieces
 //     of the same mat-vec instance (1, 2, 4, 8 or 16 token columns) share one
 //     launch, a cluster per 128-row group of an expert's piece;
 //   more rows: the tensor-core GEMM, one call per expert.
-// The switch at 24 rows is measured on GB300 for a 9728 x 2560 expert: the
-// mat-vec in pieces of 16 rows is faster up to 24 rows (19.0 us at 17 rows
-// against 22.5 us for the GEMM), the GEMM from 32 rows on (22.6 us against
-// 24.0 us).
+// The switch at 32 rows is measured on GB300 for a 9728 x 2560 expert: the
+// mat-vec in pieces of 16 rows is faster up to 32 rows (19.8 us at 17 rows
+// and 22.4 us at 32 against 24.4-24.6 us for the GEMM), the GEMM from 48 rows
+// on (24.8 us against 33.6 us).
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -48,7 +48,7 @@ extern "C" Q4MM_API int q4_0_matmul_experts(const void *const *W_packed, int64_t
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // Pieces of up to 16 rows of the experts with up to kMatvecRows rows, set
     // by set: one launch of the mat-vec per instance and per 32 pieces.
-    constexpr int64_t kMatvecRows = 24;
+    constexpr int64_t kMatvecRows = 32;
     constexpr int kInstances[5] = {1, 2, 4, 8, 16};
     int rc = Q4_OK;
     for (int inst = 0; inst < 5 && rc == Q4_OK; ++inst) {

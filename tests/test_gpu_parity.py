@@ -373,10 +373,10 @@ def test_expert_groups_match_the_oracle(q4lib, oracle_mod):
     (200, 1056, [(e * 7) % 17 for e in range(40)]),                         # two sets of <= 32
     (9728, 2560, [1, 3, 0, 16, 5, 2, 8, 4]),                                # the layer's size
     (96, 2080, [20, 1, 33, 2]),                                             # with GEMM-sized groups
-    (130, 640, [17, 24, 25, 1, 23, 40]),                                    # both sides of the 24-row switch
+    (130, 640, [17, 32, 33, 1, 23, 40]),                                    # both sides of the 32-row switch
 ])
 def test_expert_sets_match_the_oracle(q4lib, oracle_mod, n, k, sizes):
-    """Experts of up to 24 rows run the mat-vec in pieces of at most 16 rows,
+    """Experts of up to 32 rows run the mat-vec in pieces of at most 16 rows,
     pieces of one instance sharing a launch per set of up to 32 (a cluster
     per group of a piece); larger ones the GEMM. Each group is checked at its
     size's tolerance, and rows of other groups are not touched."""
