@@ -268,11 +268,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
             uint32_t at = tmem + acol0;
             int sa = 0, sb = 0;
             uint32_t pha = 0, phb = 0, acc = 0;
+            // The barrier tests for pair p + 1 are issued before pair p's
+            // MMAs: their round trip (a few hundred cycles) then overlaps
+            // the MMA issue, which blocks while the tensor pipe is busy,
+            // instead of sitting between two pairs. A pair whose tests came
+            // back negative takes the bounded wait.
+            bool ready = mbar_test_wait(&sm.full_a[0], 0u) & mbar_test_wait(&sm.full_b[0], 0u);
             for (int p = 0; p < np; ++p) {
-                if (!mbar_wait(&sm.full_a[sa], pha, a.wait_ns)) { fail(sm, a); break; }
-                trace(tr, kTrAFull, static_cast<unsigned>(p));
-                if (!mbar_wait(&sm.full_b[sb], phb, a.wait_ns)) { fail(sm, a); break; }
+                if (!ready && (!mbar_wait(&sm.full_a[sa], pha, a.wait_ns) || !mbar_wait(&sm.full_b[sb], phb, a.wait_ns))) {
+                    fail(sm, a);
+                    break;
+                }
                 trace(tr, kTrMmaIssue, static_cast<unsigned>(p));
+                int na = sa + 1, nb = sb + 1;
+                uint32_t npha = pha, nphb = phb;
+                if (na == AST) na = 0, npha ^= 1u;
+                if (nb == RB) nb = 0, nphb ^= 1u;
+                bool next = false;
+                if (p + 1 < np) next = mbar_test_wait(&sm.full_a[na], npha) & mbar_test_wait(&sm.full_b[nb], nphb);
                 tc_fence_after();
                 tc_mma_f16_ts(d, at, bd, idesc, acc);
                 tc_mma_f16_ts(d, at + 8u, bd + 2u, idesc, 1u);
@@ -281,8 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
                 tc_commit(&sm.empty_a[sa]);
                 tc_commit(&sm.empty_b[sb]);
                 acc = 1u;
-                if (++sa == AST) { sa = 0; pha ^= 1u; at = tmem + acol0; } else { at += 32u; }
-                if (++sb == RB) { sb = 0; phb ^= 1u; bd = bdesc0; } else { bd += bstep; }
+                ready = next;
+                sa = na, sb = nb, pha = npha, phb = nphb;
+                at = tmem + acol0 + 32u * static_cast<uint32_t>(sa);
+                bd = bdesc0 + static_cast<uint64_t>(sb) * bstep;
             }
             tc_commit(sm.done); // also taken on abort: no MMA of ours is in flight past this
         }
