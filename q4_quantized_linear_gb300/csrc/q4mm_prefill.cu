@@ -49,6 +49,7 @@ constexpr int kWProducerWarp = 2 + kDequantWarps;
 constexpr int kMma2Warp = 3 + kDequantWarps;
 constexpr int kWPrefetch = 8; // weight records requested into L2 beyond the ring
 constexpr int kThreads = (4 + kDequantWarps) * 32;
+constexpr size_t kStageChunkBytes = 16 * 128 * 4; // 16 tokens x 128 fp32 outputs
 
 // ------------------------------------------------------------- xcast -----
 
@@ -340,17 +341,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
         pdl_launch_dependents();
         const int chunks = T / 16;
         const int c_lo = h * ((chunks + 1) / 2), c_hi = h ? chunks : (chunks + 1) / 2;
+        // Y is row-major by token, so a token's outputs for this tile's rows
+        // are contiguous, but a warp's tensor-memory load gives each lane one
+        // row for 16 tokens. Written directly that is one 4-byte store per
+        // output, and the store instructions bound the epilogue. Staged, each
+        // warp puts its 32 rows x 16 tokens in shared memory and reads them
+        // back as 4 rows of one token per lane: four 16-byte stores per lane
+        // per chunk instead of sixteen 4-byte ones. The rings are idle by now
+        // (every X tile and weight record was consumed before the last MMA
+        // completed), so the whole tile is staged without reuse. The direct
+        // form is kept for Y whose base or row stride is not a multiple of 16
+        // bytes and for tiles too wide to stage.
+        const int64_t rows_here = min(static_cast<int64_t>(128), a.n - static_cast<int64_t>(rt) * 128);
+        const bool staged = (a.ldy & 3) == 0 && (reinterpret_cast<uintptr_t>(a.Y) & 15u) == 0 &&
+                            static_cast<size_t>(chunks) * kStageChunkBytes <=
+                                static_cast<size_t>(RB) * bstage + static_cast<size_t>(RW) * kRecordBytes;
         for (int cc = c_lo; done_ok && cc < c_hi; ++cc) {
             const int c0 = cc * 16;
             uint32_t r[16];
             tmem_ld_32x32b_x16(tmem + lane_base + static_cast<uint32_t>(c0), r);
             tmem_wait_ld();
+            if (staged) {
+                // this warp's 32 rows of the chunk: [16 tokens][32 rows]
+                uint8_t *part = sm.b + static_cast<size_t>(cc) * kStageChunkBytes + static_cast<size_t>(q) * 2048;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int tok = jt * T + c0 + i;
-                if (tok < a.m && grow < a.n) {
-                    const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[tok]) : tok;
-                    a.Y[yrow * a.ldy + grow] = __uint_as_float(r[i]);
+                for (int i = 0; i < 16; ++i) *reinterpret_cast<uint32_t *>(part + i * 128 + lane * 4) = r[i];
+                __syncwarp();
+                // lane l: rows 4 (l % 8) .. + 3 of token 4 k + l / 8
+                const int64_t col = static_cast<int64_t>(rt) * 128 + q * 32 + (lane & 7) * 4;
+                const int lrow = q * 32 + (lane & 7) * 4;   // within the 128-row tile
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = 4 * k + (lane >> 3);
+                    const int tok = jt * T + c0 + i;
+                    const uint4 v = lds128(part + i * 128 + (lane & 7) * 16);
+                    if (tok < a.m) {
+                        const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[tok]) : tok;
+                        float *dst = a.Y + yrow * a.ldy + col;
+                        if (lrow + 3 < rows_here) {
+                            *reinterpret_cast<uint4 *>(dst) = v;
+                        } else {
+                            const uint32_t e4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (lrow + e < rows_here) dst[e] = __uint_as_float(e4[e]);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int tok = jt * T + c0 + i;
+                    if (tok < a.m && grow < a.n) {
+                        const int64_t yrow = a.rows ? static_cast<int64_t>(a.rows[tok]) : tok;
+                        a.Y[yrow * a.ldy + grow] = __uint_as_float(r[i]);
+                    }
                 }
             }
         }

@@ -118,6 +118,21 @@ def test_prefill_parity(q4lib, oracle_mod, m, n, k):
     assert_parity(Y, Yr, B, m, f"prefill m={m} n={n} k={k}")
 
 
+# m = 896 over 76 row tiles plans 448-token tiles, too wide for the epilogue
+# to stage in shared memory: those CTAs store Y directly.
+@pytest.mark.parametrize("m,n,k", [(896, 9728, 256)])
+def test_prefill_wide_token_tile_sampled(q4lib, oracle_mod, m, n, k):
+    blocks = synth.q4_0_blocks(n, k, seed=31)
+    X = synth.activations(m, k, seed=32)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    r = np.random.default_rng(33)
+    t = np.concatenate([r.integers(0, m, 4000), [0, m - 1, 447, 448, m - 1]])
+    j = np.concatenate([r.integers(0, n, 4000), [0, n - 1, 127, 128, 0]])
+    Yr, B = oracle_mod.matmul_sampled(blocks, X, n, k, t, j)
+    assert_parity(Y[t, j], Yr, B, m, f"wide token tile m={m} n={n} k={k}")
+
+
 def test_library_workspace_forms(q4lib, oracle_mod):
     for (m, n, k) in [(4, 2560, 9728), (40, 300, 1024), (1, 500, 256)]:
         blocks = synth.q4_0_blocks(n, k, seed=5)
@@ -170,12 +185,16 @@ def test_workload_sizes_sampled(q4lib, oracle_mod, decode_kernel, m, n, k):
 
 # ------------------------------------------------- continuous batching ----
 
-@pytest.mark.parametrize("m,slots,n,k", [(1, 8, 300, 512), (4, 40, 9728, 2560), (16, 20, 200, 4096),
-                                         (4, 12, 2560, 9728), (20, 64, 260, 1024), (37, 40, 130, 640)])
-def test_batched_slots(q4lib, oracle_mod, decode_kernel, m, slots, n, k):
+# pad = ldy - n. With ldy a multiple of 4 and n not, the prefill epilogue's
+# 16-byte row-quad stores meet a last quad that is only partly inside Y's
+# n columns (130 = 4 * 32 + 2, 514 = 4 * 128 + 2).
+@pytest.mark.parametrize("m,slots,n,k,pad", [(1, 8, 300, 512, 5), (4, 40, 9728, 2560, 5), (16, 20, 200, 4096, 5),
+                                             (4, 12, 2560, 9728, 5), (20, 64, 260, 1024, 5), (37, 40, 130, 640, 5),
+                                             (37, 40, 130, 640, 2), (300, 320, 514, 1056, 2), (64, 64, 256, 512, 4)])
+def test_batched_slots(q4lib, oracle_mod, decode_kernel, m, slots, n, k, pad):
     once_for_prefill(decode_kernel, m)
     blocks = synth.q4_0_blocks(n, k, seed=11)
-    ldx, ldy = k + 8, n + 5
+    ldx, ldy = k + 8, n + pad
     Xs = np.zeros((slots, ldx), dtype=np.float32)
     Xs[:, :k] = synth.activations(slots, k, seed=12)
     ids = synth.slot_ids(m, slots, seed=13)
