@@ -131,7 +131,10 @@ Q4MM_API size_t q4_0_matmul_workspace_size(int64_t m, int64_t k, int64_t n);
  * W[j][c]|. For m > 16 X is rounded to bf16 (nearest even), each weight is
  * the exact (q - 8) times d rounded to bf16, rounded to bf16 (relative error
  * <= 2^-8), and the tensor cores accumulate in fp32: |Y - Y_exact| <= 1e-2 *
- * B + 1e-4. NaN and infinity in X propagate as in IEEE arithmetic.
+ * B + 1e-4 (17..32 rows, with the default decode kernel, may instead run as
+two decode calls of 16 rows and the rest, where that is estimated faster for
+the layer; they then meet the decode bound). NaN and infinity in X propagate
+as in IEEE arithmetic.
  * Scratch: this form uses a workspace the library allocates on the current
  * device, once per (device, stream), grown when a call needs more. A call
  * that has to grow it synchronises `stream` and is refused with

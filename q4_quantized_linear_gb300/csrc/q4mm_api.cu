@@ -157,6 +157,34 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     if (rc != Q4_OK) return rc;
     const uint64_t wait_ns = g_wait_ns.load();
 
+    // 17..32 rows: the mat-vec in two pieces (16 rows, then the rest) where
+    // that is estimated faster than the GEMM. golem ("Reading a prompt on
+    // the card") builds the mat-vec sixteen wide and takes tiled products
+    // from thirty-two columns; which side wins in between depends on the
+    // layer (GB300, graph replays, 17..32 rows: the GEMM takes 21 us on
+    // 9728 x 2560, 30 us on 4096 x 4096 and 65 us on 2560 x 9728, where a
+    // few 128-row groups cannot fill the SMs and K is long; the pieces
+    // 20-22, 16-19 and 23-27 us). The GEMM at these widths (token tiles of 16
+    // or 32) takes about 0.392 us per 64-deep K step and wave plus 5.4 us;
+    // the pieces, the planner's estimates of the two calls plus 3 us.
+    if (m > kDecodeMaxM && m <= 2 * kDecodeMaxM && g_decode_kernel.load() == Q4_DECODE_AUTO) {
+        MatvecPlan p16, prest;
+        PrefillPlan pp;
+        if (plan_matvec(kDecodeMaxM, k, n, dev.sm_count, &p16) &&
+            plan_matvec(m - kDecodeMaxM, k, n, dev.sm_count, &prest) && plan_prefill(m, k, n, dev.sm_count, &pp)) {
+            const double waves = static_cast<double>(
+                ceil_div(static_cast<int64_t>(pp.rowtiles) * pp.ts, static_cast<int64_t>(dev.sm_count)));
+            const double gemm_us = 0.392 * static_cast<double>(ceil_div(k, kPairK)) * waves + 5.4;
+            if (p16.est_us + prest.est_us + 3.0 < gemm_us) {
+                rc = matmul_impl(W, X, ldx, rows, Y, ldy, kDecodeMaxM, k, n, nullptr, 0, false, s);
+                if (rc != Q4_OK) return rc;
+                return matmul_impl(W, rows ? X : X + kDecodeMaxM * ldx, ldx, rows ? rows + kDecodeMaxM : nullptr,
+                                   rows ? Y : Y + kDecodeMaxM * ldy, ldy, m - kDecodeMaxM, k, n, nullptr, 0, false,
+                                   s);
+            }
+        }
+    }
+
     if (m <= kDecodeMaxM) {
         // the decode paths need no scratch: K slices meet in cluster shared memory
         DecodeArgs a{};

@@ -109,6 +109,7 @@ struct GemvPlan {
     int ctas = 0;          // clusters x S
     int ring = 8;          // weight-record ring depth (multiple of 8)
     size_t smem = 0;
+    double est_us = 0.0;   // the planner's estimate of a call back to back, in microseconds
 };
 
 bool plan_gemv(int64_t m, int64_t k, int64_t n, int sm_count, GemvPlan *plan);
@@ -157,6 +158,7 @@ struct MatvecPlan {
     int ctas = 0;          // clusters x S
     int ring = 8;          // weight-record ring depth (multiple of 8)
     size_t smem = 0;
+    double est_us = 0.0;   // the planner's estimate of a call back to back, in microseconds
 };
 
 bool plan_matvec(int64_t m, int64_t k, int64_t n, int sm_count, MatvecPlan *plan, int fmt = kMatvecQ4);

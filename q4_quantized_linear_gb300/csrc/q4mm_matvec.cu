@@ -1407,6 +1407,7 @@ bool plan_matvec_search(int M, int F, int fmt, int64_t k, int64_t n, int sm_coun
                     best.ctas = static_cast<int>(ctas);
                     best.ring = ring;
                     best.smem = smem;
+                    best.est_us = cost;
                 }
             }
         }

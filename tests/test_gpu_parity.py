@@ -58,7 +58,9 @@ def decode_kernel(request, q4lib):
 
 
 def once_for_prefill(decode_kernel, m):
-    """m > 16 never takes a decode kernel: run such a case under one of them."""
+    """m > 16 takes the GEMM under an explicitly chosen decode kernel (the
+    default dispatch may serve 17..32 rows with mat-vec pieces instead, which
+    test_pieces_dispatch covers): run such a case under one of them."""
     if m > 16 and decode_kernel != "warp_mma":
         pytest.skip("prefill case: decode kernel irrelevant")
     if decode_kernel == "cuda_core" and m > 4:
@@ -131,6 +133,39 @@ def test_prefill_wide_token_tile_sampled(q4lib, oracle_mod, m, n, k):
     j = np.concatenate([r.integers(0, n, 4000), [0, n - 1, 127, 128, 0]])
     Yr, B = oracle_mod.matmul_sampled(blocks, X, n, k, t, j)
     assert_parity(Y[t, j], Yr, B, m, f"wide token tile m={m} n={n} k={k}")
+
+
+# 17..32 rows under the default dispatch: on these layers the two mat-vec
+# pieces (16 rows, then the rest) are estimated faster than the GEMM (few
+# 128-row groups, long K), so the pieces serve them; plain rows and slot rows
+# with padded strides, against the oracle element by element.
+@pytest.mark.parametrize("m,n,k", [(17, 2560, 9728), (32, 2560, 9728), (24, 4096, 4096), (31, 260, 1024)])
+def test_pieces_dispatch(q4lib, oracle_mod, m, n, k):
+    q4lib.q4_set_decode_kernel(q4lib.Q4_DECODE_AUTO)
+    blocks = synth.q4_0_blocks(n, k, seed=41)
+    X = synth.activations(m, k, seed=42)
+    W = pack_dev(q4lib, blocks, n, k)
+    Y = run_matmul(q4lib, W, X, n)
+    Yr, B = oracle_mod.matmul(blocks, X, n, k)
+    assert_parity(Y, Yr, B, m, f"pieces m={m} n={n} k={k}")
+    slots = m + 9
+    ldx, ldy = k + 8, n + 4
+    Xs = np.zeros((slots, ldx), dtype=np.float32)
+    Xs[:, :k] = synth.activations(slots, k, seed=43)
+    ids = synth.slot_ids(m, slots, seed=44)
+    sentinel = np.float32(-12345.5)
+    Yd = torch.full((slots, ldy), float(sentinel), dtype=torch.float32, device="cuda")
+    ws, wsb = q4lib.workspace_for(m, k, n)
+    q4lib.q4_0_matmul_batched_slots_ws(W, to_dev(Xs), ldx, to_dev(ids), m, Yd, ldy, k, n, ws, wsb)
+    torch.cuda.synchronize()
+    assert q4lib.q4_last_device_status() == 0
+    Ys = Yd.cpu().numpy()
+    Yr2, B2 = oracle_mod.matmul(blocks, Xs[ids, :k], n, k)
+    assert_parity(Ys[ids, :n], Yr2, B2, m, f"pieces slots m={m}")
+    untouched = np.ones(slots, dtype=bool)
+    untouched[ids] = False
+    assert np.all(Ys[untouched] == sentinel), "rows of inactive slots were written"
+    assert np.all(Ys[ids, n:] == sentinel), "padding columns of active rows were written"
 
 
 def test_library_workspace_forms(q4lib, oracle_mod):
