@@ -161,20 +161,14 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     // that is estimated faster than the GEMM. golem ("Reading a prompt on
     // the card") builds the mat-vec sixteen wide and takes tiled products
     // from thirty-two columns; which side wins in between depends on the
-    // layer (GB300, graph replays, 17..32 rows: the GEMM takes 21 us on
-    // 9728 x 2560, 30 us on 4096 x 4096 and 65 us on 2560 x 9728, where a
-    // few 128-row groups cannot fill the SMs and K is long; the pieces
-    // 20-22, 16-19 and 23-27 us). The GEMM at these widths (token tiles of 16
-    // or 32) takes about 0.392 us per 64-deep K step and wave plus 5.4 us;
-    // the pieces, the planner's estimates of the two calls plus 3 us.
+    // layer. The two planners' estimates decide; two mat-vec calls back to
+    // back measured about 3 us above the sum of their estimates.
     if (m > kDecodeMaxM && m <= 2 * kDecodeMaxM && g_decode_kernel.load() == Q4_DECODE_AUTO) {
         MatvecPlan p16, prest;
         PrefillPlan pp;
         if (plan_matvec(kDecodeMaxM, k, n, dev.sm_count, &p16) &&
             plan_matvec(m - kDecodeMaxM, k, n, dev.sm_count, &prest) && plan_prefill(m, k, n, dev.sm_count, &pp)) {
-            const double waves = static_cast<double>(
-                ceil_div(static_cast<int64_t>(pp.rowtiles) * pp.ts, static_cast<int64_t>(dev.sm_count)));
-            const double gemm_us = 0.392 * static_cast<double>(ceil_div(k, kPairK)) * waves + 5.4;
+            const double gemm_us = pp.est_us;
             if (p16.est_us + prest.est_us + 3.0 < gemm_us) {
                 rc = matmul_impl(W, X, ldx, rows, Y, ldy, kDecodeMaxM, k, n, nullptr, 0, false, s);
                 if (rc != Q4_OK) return rc;
@@ -268,6 +262,7 @@ int matmul_impl(const void *W, const float *X, int64_t ldx, const int32_t *rows,
     pa.groups = static_cast<int>(ceil_div(n, kGroupRows));
     pa.T = plan.T;
     pa.ts = plan.ts;
+    pa.ks = plan.ks;
     pa.bring = plan.bring;
     pa.wring = plan.wring;
     pa.astages = plan.astages;

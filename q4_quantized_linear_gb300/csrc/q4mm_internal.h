@@ -200,6 +200,7 @@ struct PrefillArgs {
     uint64_t wait_ns;
     int m, n, np, groups;
     int T, ts;              // tokens per tile, token tiles
+    int ks;                 // K slices: CTAs of a cluster that share one (row tile, token tile)
     int bring;              // X-tile ring depth
     int wring;              // weight-record ring depth (even: two dequantiser sets)
     int astages;            // dequantised weight stages in tensor memory
@@ -218,11 +219,14 @@ struct XcastArgs {
 
 struct PrefillPlan {
     int T = 0, ts = 0;
+    int ks = 1;             // K slices per (row tile, token tile): the cluster size
     int rowtiles = 0;
     int bring = 0, wring = 0, astages = 0;
     size_t smem = 0;
     size_t ws_bytes = 0;    // X image bytes
+    double est_us = 0.0;    // the planner's estimate of a call, in microseconds
     size_t ws_ximg_off = 0;
+    int xcast_blocks = 0;   // grid of the X cast (grid-stride)
 };
 
 bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *plan);

@@ -35,6 +35,9 @@
 //      bandwidth to the X tiles. Every ring is an mbarrier pipeline; every
 //      wait is time-bounded.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cuda_runtime.h>
 
 #include "q4mm_device.cuh"
@@ -136,16 +139,25 @@ __device__ __forceinline__ void dequant_pair_bf16(uint32_t d01, uint4 q0, uint4 
     }
 }
 
+// SPLIT: the K slices of a tile run as one cluster and meet in its first
+// CTA; without it (a.ks == 1) the kernel carries none of that code.
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rt = blockIdx.x / a.ts; // 128-row tile = packed group
-    const int jt = blockIdx.x % a.ts; // token tile
+    // CTA = (128-row tile = packed group, token tile, K slice); the a.ks
+    // slices of a tile are one cluster and take consecutive pair ranges
+    const int KS = SPLIT ? a.ks : 1;
+    const int ksi = static_cast<int>(blockIdx.x) % KS;
+    const int tile = static_cast<int>(blockIdx.x) / KS;
+    const int rt = tile / a.ts;
+    const int jt = tile % a.ts;
     const int T = a.T;
-    const int np = a.np;
+    const int p0 = ksi * ((a.np + KS - 1) / KS);
+    const int np = min(a.np, p0 + (a.np + KS - 1) / KS) - p0; // this CTA's pairs (the planner keeps it >= 1)
     const int RB = a.bring, RW = a.wring;
     const int AST = a.astages;
     const uint32_t bstage = static_cast<uint32_t>(T) * 128u;
@@ -191,11 +203,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_slot;
 
-    const uint8_t *wsrc = a.W + static_cast<int64_t>(rt) * np * kRecordBytes;
-    const uint8_t *xsrc = a.ximg + static_cast<size_t>(jt) * np * bstage;
+    const uint8_t *wsrc = a.W + (static_cast<int64_t>(rt) * a.np + p0) * kRecordBytes;
+    const uint8_t *xsrc = a.ximg + (static_cast<size_t>(jt) * a.np + p0) * bstage;
     // One lane streams the X tiles, another (in another warp) the weight
     // records, each in pair order through its own ring (one owner per slot).
     const uint64_t pol = policy_evict_last();
+
+    // The dequantising warps (2-9) also run the epilogue: warp 2 + 4 h + i
+    // holds TMEM sub-partition q = warp % 4, i.e. weight rows 32 q .. + 31.
+    const int q = warp & 3;
+    const int h = ((warp - 2) >> 2) & 1;   // dequantiser set: pairs p % 2 == h
+    const int row = q * 32 + lane;         // weight row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const bool epi_warp = warp >= 2 && warp < 2 + kDequantWarps;
+    bool done_ok = false;
 
     if (warp == 0) {
         // ---------------------------------------------------- X-tile producer
@@ -304,12 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
         }
         __syncwarp();
     } else {
-        // ----------------------------------------------- dequantise W, epilogue
-        const int dw = warp - 2;
-        const int q = warp & 3;            // TMEM sub-partition of this warp
-        const int h = dw >> 2;             // which pairs: p % 2 == h
-        const int row = q * 32 + lane;     // weight row within the tile
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        // ----------------------------------------------------- dequantise W
         for (int p = h; p < np && !__any_sync(0xFFFFFFFFu, aborted(sm)); p += 2) {
             const int sw = p % RW, sa = p % AST;
             if (!warp_wait(&sm.full_w[sw], (p / RW) & 1, a.wait_ns)) { fail(sm, a); break; }
@@ -332,35 +348,79 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
             }
         }
 
-        // epilogue: this warp's TMEM sub-partition, half of the token columns
-        const int64_t grow = static_cast<int64_t>(rt) * 128 + row;
-        const bool done_ok = warp_wait(sm.done, 0, a.wait_ns);
+        done_ok = warp_wait(sm.done, 0, a.wait_ns);
         if (!done_ok) fail(sm, a);
         if (lane == 0) trace(tr, kTrDone, 0);
         tc_fence_after();
         pdl_launch_dependents();
-        const int chunks = T / 16;
-        const int c_lo = h * ((chunks + 1) / 2), c_hi = h ? chunks : (chunks + 1) / 2;
-        // Y is row-major by token, so a token's outputs for this tile's rows
-        // are contiguous, but a warp's tensor-memory load gives each lane one
-        // row for 16 tokens. Written directly that is one 4-byte store per
-        // output, and the store instructions bound the epilogue. Staged, each
-        // warp puts its 32 rows x 16 tokens in shared memory and reads them
-        // back as 4 rows of one token per lane: four 16-byte stores per lane
-        // per chunk instead of sixteen 4-byte ones. The rings are idle by now
-        // (every X tile and weight record was consumed before the last MMA
-        // completed), so the whole tile is staged without reuse. The direct
-        // form is kept for Y whose base or row stride is not a multiple of 16
-        // bytes and for tiles too wide to stage.
+    }
+
+    // ----------------------------------------------------------- epilogue
+    // Each dequantising warp takes its TMEM sub-partition and half of the
+    // token columns.
+    const int chunks = T / 16;
+    const int c_lo = h * ((chunks + 1) / 2), c_hi = h ? chunks : (chunks + 1) / 2;
+    const int64_t grow = static_cast<int64_t>(rt) * 128 + row;
+    // Y is row-major by token, so a token's outputs for this tile's rows
+    // are contiguous, but a warp's tensor-memory load gives each lane one
+    // row for 16 tokens. Written directly that is one 4-byte store per
+    // output, and the store instructions bound the epilogue. Staged, each
+    // warp puts its 32 rows x 16 tokens in shared memory and reads them back
+    // as 4 rows of one token per lane: four 16-byte stores per lane per
+    // chunk instead of sixteen 4-byte ones. The rings are idle by now (every
+    // X tile and weight record was consumed before the last MMA completed),
+    // so the whole tile is staged without reuse, when the staging area and
+    // the K slices' partial tiles both fit in them. The direct form is kept
+    // for Y whose base or row stride is not a multiple of 16 bytes and for
+    // tiles too wide to stage. (Uniform over the cluster: its CTAs agree on
+    // where the partial tiles go.)
+    const size_t ring_bytes = static_cast<size_t>(RB) * bstage + static_cast<size_t>(RW) * kRecordBytes;
+    const bool staged = (a.ldy & 3) == 0 && (reinterpret_cast<uintptr_t>(a.Y) & 15u) == 0 &&
+                        static_cast<size_t>(KS) * chunks * kStageChunkBytes <= ring_bytes;
+    // Partial tiles of slices 1 .. KS - 1, [slice - 1][token column][row]
+    // fp32, in the first CTA's rings: after the staging area when staged,
+    // else from the start (the planner keeps them inside the rings).
+    const size_t partial_off = staged ? static_cast<size_t>(chunks) * kStageChunkBytes : 0;
+    float *partials = reinterpret_cast<float *>(sm.b + partial_off);
+    if (SPLIT && !q4_check(partial_off + static_cast<size_t>(KS - 1) * chunks * kStageChunkBytes <= ring_bytes, a.status))
+        done_ok = false; // (checked build) no partial tile is written or read
+    if constexpr (SPLIT) {
+        // Every CTA of the cluster has left its K loop (the first CTA's
+        // rings are free); every thread passes both barriers, also after a
+        // failed wait, so that none is left at one.
+        tc_fence_before();
+        cluster_sync();
+        tc_fence_after();
+        if (epi_warp && ksi > 0 && done_ok) {
+            const uint32_t dst0 = mapa_shared(smem_u32(partials), 0u) +
+                                  static_cast<uint32_t>((static_cast<size_t>(ksi - 1) * T * 128 + row) * 4);
+            for (int cc = c_lo; cc < c_hi; ++cc) {
+                const int c0 = cc * 16;
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(tmem + lane_base + static_cast<uint32_t>(c0), r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    st_cluster_f32(dst0 + static_cast<uint32_t>((c0 + i) * 128 * 4), __uint_as_float(r[i]));
+            }
+        }
+        tc_fence_before();
+        cluster_sync(); // the partial tiles are in the first CTA's shared memory
+        tc_fence_after();
+    }
+    if (epi_warp && ksi == 0 && done_ok) {
         const int64_t rows_here = min(static_cast<int64_t>(128), a.n - static_cast<int64_t>(rt) * 128);
-        const bool staged = (a.ldy & 3) == 0 && (reinterpret_cast<uintptr_t>(a.Y) & 15u) == 0 &&
-                            static_cast<size_t>(chunks) * kStageChunkBytes <=
-                                static_cast<size_t>(RB) * bstage + static_cast<size_t>(RW) * kRecordBytes;
-        for (int cc = c_lo; done_ok && cc < c_hi; ++cc) {
+        for (int cc = c_lo; cc < c_hi; ++cc) {
             const int c0 = cc * 16;
             uint32_t r[16];
             tmem_ld_32x32b_x16(tmem + lane_base + static_cast<uint32_t>(c0), r);
             tmem_wait_ld();
+            // the other K slices' partial sums, in slice order
+            for (int sl = 0; SPLIT && sl + 1 < KS; ++sl) {
+                const float *pt = partials + (static_cast<size_t>(sl) * T + c0) * 128 + row;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + pt[i * 128]);
+            }
             if (staged) {
                 // this warp's 32 rows of the chunk: [16 tokens][32 rows]
                 uint8_t *part = sm.b + static_cast<size_t>(cc) * kStageChunkBytes + static_cast<size_t>(q) * 2048;
@@ -399,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const PrefillArgs a)
                 }
             }
         }
-        if (lane == 0) trace(tr, kTrEpiDone, 0);
     }
+    if (epi_warp && lane == 0) trace(tr, kTrEpiDone, 0);
 
     tc_fence_before();
     __syncthreads();
@@ -431,13 +491,81 @@ size_t gemm_smem_bytes(int T, int bring, int wring, int astages)
            16;
 }
 
+// Clusters of ks GEMM CTAs (`threads` each, `smem` bytes of dynamic shared
+// memory) that the current device holds at once; 0 when it cannot be asked.
+// Cached per (device, ks, smem, threads).
+int gemm_max_clusters(int ks, size_t smem, int threads)
+{
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, size_t, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const auto key = std::make_tuple(dev, ks, smem, threads);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const void *fn = reinterpret_cast<const void *>(&gemm_kernel<true>);
+    int n = 0;
+    if (set_max_smem(fn, smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(ks));
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(ks);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cache.emplace(key, n);
+    return n;
+}
+
 } // namespace
 
-// Choose the token tile T (multiple of 16, at most 448 so tensor memory keeps
-// room for two weight stages) and the number of token tiles so that
-// (128-row tiles) x (token tiles) fills the SMs in as few waves as possible;
-// then the rings that fit in shared memory.
-bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *plan)
+namespace {
+
+// Rings and tensor-memory stages for a token tile of T; false when none fits.
+bool prefill_rings(int T, PrefillPlan *p)
+{
+    const int acol0 = (T + 31) & ~31;
+    // even, so that each stage always belongs to one of the two dequantiser
+    // sets (parity waits need a single waiter per barrier)
+    p->astages = std::min(8, (512 - acol0) / 32) & ~1;
+    if (p->astages < 2) return false;
+    // A weight ring of 8 first (the records come from HBM, the X tiles from
+    // L2: for 540x9728x2560 a ring of 8 next to 5 X tiles beats 4 next to 6
+    // by 4%), then the deepest X-tile ring that fits next to it.
+    p->bring = p->wring = 0;
+    for (int wr : {8, 4, 2}) {
+        int br = 8;
+        while (br > 2 && gemm_smem_bytes(T, br, wr, p->astages) > kSmemOptIn) --br;
+        if (gemm_smem_bytes(T, br, wr, p->astages) > kSmemOptIn) continue;
+        if (wr > p->wring) p->bring = br, p->wring = wr;
+    }
+    if (p->bring == 0) return false;
+    p->smem = gemm_smem_bytes(T, p->bring, p->wring, p->astages);
+    if (p->smem > kSmemOptIn) return false;
+    // one CTA per SM: each holds all 512 tensor-memory columns
+    p->smem = std::max<size_t>(p->smem, kSmemPerSM / 2 + 1024);
+    return true;
+}
+
+// Time model of a call, fitted to graph-replay timings on GB300: a CTA's
+// 64-deep K step takes about the same whatever the token tile (0.39 us at
+// 16 tokens, 0.43 at 144, 0.45 at 272: the dequantisation and the MMA issue
+// set it, not the tensor math), plus a fixed 5 us per wave; a K split adds
+// its exchange, and the direct epilogue (no room to stage) its stores.
+constexpr double kPairUs = 0.42, kWaveUs = 5.0, kSplitUs = 1.0, kDirectUs = 1.3;
+
+bool plan_prefill_search(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *plan)
 {
     const int64_t rowtiles = ceil_div(n, kGroupRows);
     const int64_t np = ceil_div(k, kPairK);
@@ -446,40 +574,86 @@ bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *pl
     for (int64_t ts = ceil_div(m, 448); ts <= std::max<int64_t>(1, ceil_div(m, 16)); ++ts) {
         const int64_t T = round_up(ceil_div(m, ts), 16);
         if (T > 448) continue;
-        const int64_t ctas = rowtiles * ts;
-        const int64_t waves = ceil_div(ctas, sm_count);
-        const double cost = static_cast<double>(waves) * (static_cast<double>(T) + 48.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best.T = static_cast<int>(T);
-            best.ts = static_cast<int>(ts);
+        PrefillPlan c;
+        c.T = static_cast<int>(T);
+        c.ts = static_cast<int>(ts);
+        c.rowtiles = static_cast<int>(rowtiles);
+        if (!prefill_rings(c.T, &c)) continue;
+        const size_t cap = static_cast<size_t>(c.bring) * c.T * 128 + static_cast<size_t>(c.wring) * kRecordBytes;
+        const int threads = c.T >= 32 ? kThreads : kThreads - 32;
+        const int64_t tiles = rowtiles * ts;
+        // ks K slices: a cluster of ks CTAs per tile; the first CTA sums the
+        // others' partial tiles, which must fit in its rings (with the
+        // staging area too for the staged epilogue); every slice non-empty
+        // and at least 4 pairs long
+        for (int ks = 1; ks <= 8; ++ks) {
+            int64_t waves = ceil_div(tiles, static_cast<int64_t>(sm_count));
+            if (ks > 1) {
+                if (np < 8 || ks > np / 4) break;
+                if ((ks - 1) * ceil_div(np, ks) >= np) continue;
+                if (static_cast<size_t>(ks - 1) * c.T * 512 > cap) continue;
+                const int mc = gemm_max_clusters(ks, c.smem, threads);
+                if (mc < 1) continue;
+                waves = ceil_div(tiles, static_cast<int64_t>(mc));
+            }
+            const bool staged = static_cast<size_t>(ks) * c.T * 512 <= cap;
+            const double cost = static_cast<double>(waves) * (kPairUs * static_cast<double>(ceil_div(np, ks)) + kWaveUs) +
+                                (ks > 1 ? kSplitUs : 0.0) + (staged ? 0.0 : kDirectUs * c.T / 272.0);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best = c;
+                best.ks = ks;
+            }
         }
         if (ts > 4096) break;
     }
     if (best.T == 0) return false;
-    best.rowtiles = static_cast<int>(rowtiles);
-    const int acol0 = (best.T + 31) & ~31;
-    // even, so that each stage always belongs to one of the two dequantiser
-    // sets (parity waits need a single waiter per barrier)
-    best.astages = std::min(8, (512 - acol0) / 32) & ~1;
-    if (best.astages < 2) return false;
-    // A weight ring of 8 first (the records come from HBM, the X tiles from
-    // L2: for 540x9728x2560 a ring of 8 next to 5 X tiles beats 4 next to 6
-    // by 4%), then the deepest X-tile ring that fits next to it.
-    for (int wr : {8, 4, 2}) {
-        int br = 8;
-        while (br > 2 && gemm_smem_bytes(best.T, br, wr, best.astages) > kSmemOptIn) --br;
-        if (gemm_smem_bytes(best.T, br, wr, best.astages) > kSmemOptIn) continue;
-        if (wr > best.wring) best.bring = br, best.wring = wr;
-    }
-    if (best.bring == 0) return false;
-    best.smem = gemm_smem_bytes(best.T, best.bring, best.wring, best.astages);
-    if (best.smem > kSmemOptIn) return false;
-    // one CTA per SM: each holds all 512 tensor-memory columns
-    best.smem = std::max<size_t>(best.smem, kSmemPerSM / 2 + 1024);
+    best.est_us = best_cost;
+    // Two blocks per SM: they run beside the GEMM CTA of the preceding call
+    // (launched early, each waiting for that call to end) in one wave
+    // whatever registers the GEMM holds; each thread converts several items.
+    best.xcast_blocks = static_cast<int>(std::min<int64_t>(
+        ceil_div(static_cast<int64_t>(best.ts) * np * best.T * 8, 256), 2 * static_cast<int64_t>(sm_count)));
     best.ws_ximg_off = 0;
     best.ws_bytes = static_cast<size_t>(best.ts) * np * best.T * 128;
     *plan = best;
+    return true;
+}
+
+} // namespace
+
+// Choose the token tile T (multiple of 16, at most 448 so that tensor memory
+// keeps room for two weight stages), the number of token tiles and the K
+// slices by the time model above, then the rings that fit in shared memory.
+// Computed once per (device, shape, SM count).
+bool plan_prefill(int64_t m, int64_t k, int64_t n, int sm_count, PrefillPlan *plan)
+{
+    if (m < 1 || sm_count < 1) return false;
+    static std::mutex mu;
+    static std::map<std::tuple<int, int64_t, int64_t, int64_t, int>, PrefillPlan> cache;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        dev = -1;
+    }
+    const auto key = std::make_tuple(dev, m, k, n, sm_count);
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            if (it->second.T == 0) return false;
+            *plan = it->second;
+            return true;
+        }
+    }
+    PrefillPlan found;
+    const bool ok = plan_prefill_search(m, k, n, sm_count, &found);
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache.emplace(key, ok ? found : PrefillPlan{});
+    }
+    if (!ok) return false;
+    *plan = found;
     return true;
 }
 
@@ -488,13 +662,13 @@ cudaError_t launch_prefill(const PrefillPlan &plan, const XcastArgs &xa, const P
     {
         XcastArgs a = xa;
         void *kargs[] = {&a};
-        const int64_t total = static_cast<int64_t>(xa.ts) * xa.np * xa.T * 8;
-        const int64_t grid = std::min<int64_t>(ceil_div(total, 256), 65535);
+        const int64_t grid = std::max(1, plan.xcast_blocks);
         cudaError_t e = launch_pdl(reinterpret_cast<const void *>(&xcast_kernel), dim3(static_cast<unsigned>(grid)),
                                    dim3(256), 0, s, kargs);
         if (e != cudaSuccess) return e;
     }
-    const void *fn = reinterpret_cast<const void *>(&gemm_kernel);
+    const void *fn = plan.ks > 1 ? reinterpret_cast<const void *>(&gemm_kernel<true>)
+                                 : reinterpret_cast<const void *>(&gemm_kernel<false>);
     cudaError_t e = set_max_smem(fn, plan.smem);
     if (e != cudaSuccess) return e;
     PrefillArgs a = pa;
@@ -505,7 +679,8 @@ cudaError_t launch_prefill(const PrefillPlan &plan, const XcastArgs &xa, const P
     void *kargs[] = {&a};
     // warp 11 exists only when the tile takes two MMA threads (T >= 32)
     const int threads = plan.T >= 32 ? kThreads : kThreads - 32;
-    return launch_pdl(fn, dim3(static_cast<unsigned>(plan.rowtiles * plan.ts)), dim3(threads), plan.smem, s, kargs);
+    return launch_pdl(fn, dim3(static_cast<unsigned>(plan.rowtiles * plan.ts * plan.ks)), dim3(threads), plan.smem, s,
+                      kargs, plan.ks);
 }
 
 cudaError_t launch_wait_selftest(int *status, uint64_t limit_ns, cudaStream_t s)
