@@ -135,10 +135,10 @@ def test_prefill_wide_token_tile_sampled(q4lib, oracle_mod, m, n, k):
     assert_parity(Y[t, j], Yr, B, m, f"wide token tile m={m} n={n} k={k}")
 
 
-# 17..32 rows under the default dispatch: on these layers the two mat-vec
-# pieces (16 rows, then the rest) are estimated faster than the GEMM (few
-# 128-row groups, long K), so the pieces serve them; plain rows and slot rows
-# with padded strides, against the oracle element by element.
+# 17..32 rows under the default dispatch, which runs either the GEMM (with a
+# K split on layers of few 128-row groups) or two mat-vec calls (16 rows,
+# then the rest), whichever the planners estimate faster; plain rows and
+# slot rows with padded strides, against the oracle element by element.
 @pytest.mark.parametrize("m,n,k", [(17, 2560, 9728), (32, 2560, 9728), (24, 4096, 4096), (31, 260, 1024)])
 def test_pieces_dispatch(q4lib, oracle_mod, m, n, k):
     q4lib.q4_set_decode_kernel(q4lib.Q4_DECODE_AUTO)
