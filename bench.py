@@ -71,6 +71,8 @@ SWEEP = [
     dict(name="slot sweep 14336x4096", m=16, n=14336, k=4096),
     dict(name="logit head", m=4, n=151936, k=2560),
     dict(name="prefill", m=540, n=9728, k=2560),
+    # prefill of a down-projection: 20 row groups, K split across clusters
+    dict(name="prefill, down-projection (K split)", m=540, n=2560, k=9728),
     # the integer-dot variant (q4_0_matmul_w4a8): X coded to int8 per block
     dict(name="W4A8 decode up-projection", m=1, n=9728, k=2560, w4a8=True),
     dict(name="W4A8 slot sweep 14336x4096", m=8, n=14336, k=4096, w4a8=True),
